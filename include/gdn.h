@@ -1,0 +1,196 @@
+/*
+ * gdn.h — C ABI of the packed gated-delta-rule (GDN) prefill library for sm_103a.
+ *
+ * What the library computes
+ * -------------------------
+ * The gated delta rule (Gated Delta Networks, Yang, Kautz & Hatamizadeh, 2024) is the
+ * linear-attention layer of the Qwen3.5/3.6 hybrid models ("hybrid attention architecture
+ * used by Qwen3.5-style models", vLLM-Ascend tutorial "Qwen3.6-35B-A3B", §1 Introduction).
+ * For every packed prompt n and value head h, with key head hk = h / (H_v / H_k), the
+ * state S (d_v x d_k, fp32) evolves token by token:
+ *
+ *     q_t, k_t <- q_t / ||q_t||, k_t / ||k_t||          (when qk_l2norm != 0)
+ *     g_t = exp(a_t)
+ *     S_t = g_t S_{t-1} - beta_t (g_t S_{t-1} k_t - v_t) k_t^T
+ *     o_t = scale * S_t q_t
+ *
+ * Many prompts share one pass ("packed passes", sparkinfer v0.6.28 release notes, intro).
+ * Each prompt may start from its own initial state (a prefix-cache hit) and the pass emits
+ * state snapshots at requested prompt positions ("prefix-cache checkpoint", same release
+ * notes, bullets 2-4). A one-token decode update serves sequences that are decoding
+ * ("packed GDN decode", vllm.cpp "vLLM, online serving", lever 2b).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer named *_host is host memory; every other data pointer is device memory
+ *    of the current CUDA device, owned by the caller, and must stay valid until the work
+ *    queued on `stream` has finished. The library never frees caller memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). All
+ *    device work is asynchronous on it.
+ *  - All arguments are validated on the host before anything is enqueued; on an error
+ *    nothing is launched and the status says why ("reject unsupported combinations before
+ *    model loading", pegainfer PR #786, Changes). A failed launch returns GDN_ERR_CUDA.
+ *  - No call logs, throws or exits.
+ *  - Token-major layouts: q, k are [T][H_k][d_k]; v, o are [T][H_v][d_v]; a and beta are
+ *    [T][H_v]; states are [.][H_v][d_v][d_k] fp32 with d_k contiguous (row = value dim).
+ *    T = cu_seqlens_host[num_seqs]. Device buffers must be 16-byte aligned.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_ABI_VERSION 1
+
+typedef enum gdn_status {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARGUMENT = 1,   /* malformed sizes, pointers, offsets or positions  */
+  GDN_ERR_UNSUPPORTED = 2,        /* well-formed but outside what the kernels cover   */
+  GDN_ERR_WORKSPACE_TOO_SMALL = 3,
+  GDN_ERR_CUDA = 4,               /* a CUDA runtime call or launch failed             */
+  GDN_ERR_DEVICE_TIMEOUT = 5,     /* a bounded device-side wait gave up               */
+  GDN_ERR_POOL_EXHAUSTED = 6      /* pinned snapshot pool range out of bounds         */
+} gdn_status;
+
+typedef enum gdn_dtype {
+  GDN_F32 = 0,   /* q, k, v, o in fp32 */
+  GDN_BF16 = 1   /* q, k, v, o in bf16; a, beta and all states stay fp32 */
+} gdn_dtype;
+
+/* Layer shape. Supported: head_dim_k == head_dim_v in {64, 128}, num_v_heads a positive
+ * multiple of num_k_heads, chunk_size == 64. */
+typedef struct gdn_config {
+  int32_t num_k_heads;   /* H_k */
+  int32_t num_v_heads;   /* H_v; value head h reads key head h / (H_v / H_k)       */
+  int32_t head_dim_k;    /* d_k */
+  int32_t head_dim_v;    /* d_v */
+  int32_t chunk_size;    /* C: token block of the chunked scan; checkpoint grid     */
+  float scale;           /* output scale, usually 1/sqrt(d_k)                       */
+  int32_t qk_l2norm;     /* nonzero: q, k <- x / sqrt(x.x + 1e-6) per token and head */
+  int32_t io_dtype;      /* gdn_dtype of q, k, v, o                                 */
+} gdn_config;
+
+typedef struct gdn_handle gdn_handle;
+
+/* Library ABI version (GDN_ABI_VERSION of the build). */
+int32_t gdn_abi_version(void);
+
+/* Static, NUL-terminated name of a status code; unknown codes give "unknown status". */
+const char* gdn_status_string(int32_t status);
+
+/* Create a handle bound to CUDA device `device`. The handle owns a pinned host snapshot
+ * pool of `pinned_pool_bytes` (0 = none), allocated here, once, rather than in the middle
+ * of a pass (sparkinfer v0.6.28, bullet on pinned host buffers), a side stream for
+ * checkpoint copies, a pinned staging ring for work lists, and events. On success *out
+ * receives the handle. Errors: INVALID_ARGUMENT (out NULL, device out of range), CUDA. */
+gdn_status gdn_handle_create(int32_t device, size_t pinned_pool_bytes, gdn_handle** out);
+
+/* Drain the handle's side stream and staging ring, then free what the handle owns
+ * ("drain the prefill stream on error, cancellation, drop, and shutdown", pegainfer PR
+ * #786, Changes). NULL is accepted and ignored. */
+gdn_status gdn_handle_destroy(gdn_handle* handle);
+
+/* Host address and size of the handle's pinned snapshot pool. */
+gdn_status gdn_pool_info(gdn_handle* handle, void** host_ptr, size_t* bytes);
+
+/* Device workspace bytes that gdn_prefill_packed needs for this pack (the chunk/tile work
+ * list). Validates the same arguments gdn_prefill_packed validates about the pack.
+ * Result is a multiple of 256 and at least 256. */
+gdn_status gdn_prefill_workspace_size(const gdn_config* cfg, int32_t num_seqs,
+                                      const int32_t* cu_seqlens_host,
+                                      const int32_t* ckpt_cu_host, size_t* bytes);
+
+/* Packed variable-length prefill of the gated delta rule.
+ *
+ *  num_seqs         N >= 1 prompts in the pack.
+ *  cu_seqlens_host  [N+1] int32, cu[0] = 0, non-decreasing; prompt n is tokens
+ *                   [cu[n], cu[n+1]). Zero-length prompts are allowed: their final state
+ *                   is their initial state and they emit no output.
+ *  q, k             [T][H_k][d] io_dtype.   v: [T][H_v][d] io_dtype.
+ *  a, beta          [T][H_v] fp32: log-decay (g = exp(a), a <= 0) and the write strength.
+ *  initial_state    [N][H_v][d][d] fp32, or NULL for all-zero initial states.
+ *  ckpt_cu_host     [N+1] int32 CSR over ckpt_pos_host (ckpt_cu[0] = 0), or NULL when no
+ *                   prompt asks for a checkpoint.
+ *  ckpt_pos_host    prompt-relative positions p: the snapshot is the state after the first
+ *                   p tokens of that prompt's segment. Per prompt strictly increasing, in
+ *                   [1, len], and each a multiple of chunk_size or equal to len
+ *                   (otherwise GDN_ERR_UNSUPPORTED).
+ *  o                [T][H_v][d] io_dtype output.
+ *  ckpt_states      [ckpt_cu[N]][H_v][d][d] fp32; slot j holds checkpoint j of the CSR.
+ *                   May be NULL only when there is no checkpoint.
+ *  final_states     [N][H_v][d][d] fp32 state after each prompt's last token. May equal
+ *                   initial_state (in-place update); no other overlap is allowed.
+ *  workspace        device scratch of at least gdn_prefill_workspace_size() bytes,
+ *                   256-byte aligned; it must not be reused by other work before this
+ *                   call's work on `stream` has finished.
+ * The result does not depend on how prompts are packed: each prompt's outputs, checkpoints
+ * and final state are bit-identical whether it runs alone or inside any pack ("the same
+ * checkpoints whether prompts are prefilled alone or packed", sparkinfer v0.6.28,
+ * pack_ckpt_check). Errors: INVALID_ARGUMENT, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA. */
+gdn_status gdn_prefill_packed(gdn_handle* handle, const gdn_config* cfg, int32_t num_seqs,
+                              const int32_t* cu_seqlens_host,
+                              const void* q, const void* k, const void* v,
+                              const float* a, const float* beta,
+                              const float* initial_state,
+                              const int32_t* ckpt_cu_host, const int32_t* ckpt_pos_host,
+                              void* o, float* ckpt_states, float* final_states,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Copy `bytes` of device checkpoint states into the handle's pinned pool at byte offset
+ * `pool_offset`, on the handle's side stream, after all work already queued on `stream`
+ * (so the scan and the copy of the next prompts overlap; sparkinfer v0.6.28, bullet on
+ * separate streams for the scan and the checkpoint copy). Returns at once; completion is
+ * observed with gdn_checkpoint_copy_query / _wait. Errors: INVALID_ARGUMENT,
+ * POOL_EXHAUSTED (range outside the pool), CUDA. */
+gdn_status gdn_checkpoint_copy(gdn_handle* handle, const float* ckpt_states_dev, size_t bytes,
+                               size_t pool_offset, void* stream);
+
+/* GDN_OK when every checkpoint copy issued so far has completed, otherwise
+ * GDN_ERR_DEVICE_TIMEOUT (not finished yet; nothing is wrong). */
+gdn_status gdn_checkpoint_copy_query(gdn_handle* handle);
+
+/* Block the calling host thread until every checkpoint copy issued so far has completed. */
+gdn_status gdn_checkpoint_copy_wait(gdn_handle* handle);
+
+/* One-token decode update for `batch` decoding sequences, each with its own fp32 state in
+ * a caller-owned pool, updated in place (vllm.cpp "vLLM, online serving", packed GDN
+ * decode lever). For sequence b:
+ *     S = state_pool[slot_idx[b]]   ([H_v][d][d] fp32 per slot)
+ *     one step of the recurrence with q[b], k[b] ([batch][H_k][d]), v[b] ([batch][H_v][d]),
+ *     a[b], beta[b] ([batch][H_v] fp32); o[b] ([batch][H_v][d] io_dtype) = scale * S_new q
+ *  slot_idx_dev     [batch] int32 device array of distinct slot indices in [0, num_slots).
+ * Distinct slots are the caller's duty (two batch rows naming one slot race).
+ * Errors: INVALID_ARGUMENT, UNSUPPORTED, CUDA. */
+gdn_status gdn_decode_step(gdn_handle* handle, const gdn_config* cfg, int32_t batch,
+                           const void* q, const void* k, const void* v,
+                           const float* a, const float* beta,
+                           float* state_pool, int32_t num_slots, const int32_t* slot_idx_dev,
+                           void* o, void* stream);
+
+/* ---- host-side scheduling policy (no device work) ---------------------------------- */
+
+/* Prefix-cache checkpoint position of a prompt of `len` tokens on a grid of `block`
+ * tokens: the last multiple of `block` that is <= len, moved back one block when it falls
+ * within the prompt's last `tail` tokens, so the prompt can stay in the pack (sparkinfer
+ * v0.6.28, bullet on checkpoints in the last 16 tokens; there tail = 16). Returns the
+ * position, or 0 when no checkpoint remains (len < block after the move). */
+int32_t gdn_ckpt_position(int32_t len, int32_t block, int32_t tail);
+
+/* Mixed-step prompt budget (sparkinfer v0.6.4 release notes, "What changed"): walk the
+ * waiting prompts oldest first (index order), at most `max_prompts` of them, giving each
+ * min(remaining_i, budget_left) tokens until `budget` tokens are used. take_out[i]
+ * receives prompt i's share (0 for prompts not served). Returns the number of prompts
+ * served, or -1 on invalid arguments. */
+int32_t gdn_mixed_budget(int32_t num_waiting, const int32_t* remaining_host, int32_t budget,
+                         int32_t max_prompts, int32_t* take_out_host);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */
