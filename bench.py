@@ -1,0 +1,347 @@
+#!/usr/bin/env python3
+"""Packed GDN prefill throughput on the 32 x 1,024 chat wave (tokens/s, % of roofline).
+
+One step = one gdn_prefill_packed call over the whole wave: 32 prompts of 1,024 tokens
+packed into one pass (32,768 tokens), H_k = 16, H_v = 32, d_k = d_v = 128, bf16 q/k/v/o,
+fp32 gates and states, one prefix-cache checkpoint per prompt (position 768: the last
+multiple of 256 moved back out of the last 16 tokens) plus the final states. Inputs are
+synthetic and seeded (packed_linear_attention_gb300.inputs), resident in HBM before the
+timed region; they are larger than L2 and L2 is also flushed between timed steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own wave (independent prompts: weak scaling,
+no collective on the data path); rank 0 prints one JSON line with the max-over-ranks time.
+`--impl reference` times the CPU oracle (the only other implementation) on a bounded
+sample of the same workload on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN packed-prefill tokens/s at 32x1024 (1 GB300) + % of roofline"
+UNIT = "tokens/s"
+WORKLOAD = dict(workload="chat_wave_32x1024", prompts=32, prompt_len=1024, tokens=32768,
+                num_k_heads=16, num_v_heads=32, head_dim=128, chunk=64,
+                checkpoints="768 per prompt + final", io="bf16 qkv/o, fp32 gates+states",
+                l2="inputs > L2 and L2 flushed between timed steps")
+
+
+def algorithmic_bytes(T, Hk, Hv, d, n_seqs, n_ckpt, s_in=2, s_out=2, init=False):
+    """Bytes the method must move: read q, k, v, a, beta (and initial states if given),
+    write o, checkpoints and final states. Intermediates are not counted."""
+    b = 2 * T * Hk * d * s_in + T * Hv * d * s_in + 2 * T * Hv * 4 + T * Hv * d * s_out
+    if init:
+        b += n_seqs * Hv * d * d * 4
+    b += (n_ckpt + n_seqs) * Hv * d * d * 4
+    return b
+
+
+def algorithmic_flops(T, Hk, Hv, d, C=64):
+    """Dense tensor-core flops of the chunked method per pass: per token and value head
+    6 d^2 (three state products) + 6 C d (W, U and the intra-chunk output), plus
+    K K^T and Q K^T (2 C d each) once per token and key head."""
+    return T * Hv * (6 * d * d + 6 * C * d) + T * Hk * (4 * C * d)
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self._t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self._t:
+                self._t.join(timeout=2)
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---- CPU oracle (baseline / reference arm) -------------------------------------------------
+
+def oracle_rate(pack, n_prompts: int, n_heads: int, threads: int):
+    """Time the fp64 oracle on `n_prompts` prompts x `n_heads` value heads of the wave;
+    returns (full-layer tokens/s, seconds, sample description)."""
+    from oracle import ref
+    from packed_linear_attention_gb300 import inputs as I
+    heads = list(range(n_heads))
+    sub = I.sub_pack(pack, list(range(n_prompts)), heads)
+    args = (sub.cu_seqlens, sub.as_f32("q"), sub.as_f32("k"), sub.as_f32("v"), sub.a, sub.beta,
+            sub.init, sub.ckpt_cu, sub.ckpt_pos)
+    t0 = time.perf_counter()
+    ref.prefill_arrays(*args, scale=sub.scale, threads=threads)
+    dt = time.perf_counter() - t0
+    layer_tokens = sub.total_tokens * n_heads / pack.num_v_heads
+    desc = (f"{n_prompts} prompt(s) x 1024 tokens x {n_heads}/{pack.num_v_heads} value heads "
+            f"of the wave, fp64 token-by-token oracle, {threads} threads; tokens/s scaled to "
+            f"all {pack.num_v_heads} heads")
+    return layer_tokens / dt, dt, desc
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from packed_linear_attention_gb300 import inputs as I
+    pack = I.chat_wave()
+    threads = os.cpu_count() or 1
+    n_heads = 8
+    for _ in range(args.warmup):
+        oracle_rate(pack, 1, n_heads, threads)
+    times, desc = [], ""
+    for _ in range(args.steps):
+        _, dt, desc = oracle_rate(pack, 1, n_heads, threads)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    layer_tokens = 1024 * n_heads / pack.num_v_heads
+    value = layer_tokens / (ms / 1e3)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": WORKLOAD,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+    return 0
+
+
+# ---- GPU arm --------------------------------------------------------------------------------
+
+def run_gpu(args):
+    import torch
+
+    from packed_linear_attention_gb300 import build, gdn
+    from packed_linear_attention_gb300 import inputs as I
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    build.build()
+    pack = I.chat_wave(seed=rank)  # each rank: its own independent wave
+    T, Hk, Hv, d, N = pack.total_tokens, 16, 32, 128, pack.num_seqs
+    h = gdn.gdn_handle_create(dev.index, 256 << 20)
+    buf = gdn.to_device(pack, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MiB > 129 MB L2
+
+    def step():
+        gdn.prefill(h, buf, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert gdn.gdn_read_device_status(buf.workspace) == 0
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_local = sum(per) / len(per)
+    ms = reduce_max(ms_local, world, dev)
+    value = T * world / (ms / 1e3)
+
+    # roofline of the prefill kernel (the only kernel of the step)
+    hbm_gbs, tflops, peak_src = load_peaks()
+    B = algorithmic_bytes(T, Hk, Hv, d, N, pack.num_ckpts)
+    F = algorithmic_flops(T, Hk, Hv, d)
+    achieved = B / (ms_local / 1e3) / 1e9
+    t_hbm = B / (hbm_gbs * 1e9)
+    t_tc = F / (tflops * 1e12)
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+            "frac": achieved / hbm_gbs, "traffic": None,
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst copy)",
+            "algorithmic_bytes": B, "algorithmic_flops": F,
+            "t_roof_us": max(t_hbm, t_tc) * 1e6, "t_hbm_us": t_hbm * 1e6,
+            "t_tensor_us": t_tc * 1e6, "kernel_us": ms_local * 1e3,
+            "frac_of_roofline": max(t_hbm, t_tc) / (ms_local / 1e3)}
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, torch, gdn, h, buf, pack, stream, world, dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        rate, dt, desc = oracle_rate(pack, args.cpu_prompts, 32, threads)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": desc + f" ({dt:.1f} s)"}
+
+    gdn.gdn_handle_destroy(h)
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": dict(WORKLOAD, parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps, "clocks": clocks.summary(),
+        }), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, torch, gdn, h, buf, pack, stream, world, dev):
+    """Host-resident inputs: per step, pinned H2D of q, k, v, a, beta, the prefill call,
+    D2H of o and the final states into pinned memory, and the checkpoint copy into the
+    handle's pinned snapshot pool on its side stream."""
+    host = {}
+    for name in ("q", "k", "v", "a", "beta"):
+        t = getattr(buf, name)
+        host[name] = t.cpu().pin_memory()
+    o_host = torch.empty(buf.o.shape, dtype=buf.o.dtype).pin_memory()
+    f_host = torch.empty(buf.final.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host.values())
+    ck_bytes = buf.ckpt.numel() * 4
+    d2h = o_host.numel() * o_host.element_size() + f_host.numel() * 4 + ck_bytes
+
+    def step():
+        for name, t in host.items():
+            getattr(buf, name).copy_(t, non_blocking=True)
+        gdn.prefill(h, buf, stream)
+        gdn.gdn_checkpoint_copy(h, buf.ckpt, ck_bytes, 0, stream)
+        o_host.copy_(buf.o, non_blocking=True)
+        f_host.copy_(buf.final, non_blocking=True)
+        torch.cuda.synchronize()
+        gdn.gdn_checkpoint_copy_wait(h)
+
+    for _ in range(2):
+        step()
+    steps = max(3, min(args.steps, 10))
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = (time.perf_counter() - t0) / steps
+    dt = reduce_max(dt, world, dev)
+    return {"value": pack.total_tokens * world / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
+    ap.add_argument("--cpu-prompts", type=int, default=32,
+                    help="prompts of the wave in the timed CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

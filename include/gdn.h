@@ -98,6 +98,12 @@ gdn_status gdn_handle_destroy(gdn_handle* handle);
 /* Host address and size of the handle's pinned snapshot pool. */
 gdn_status gdn_pool_info(gdn_handle* handle, void** host_ptr, size_t* bytes);
 
+/* Kernel choice for later prefill calls on this handle: 0 = automatic (the tensor-core
+ * chunked kernel where it applies: bf16 io, d = 128; otherwise the token-serial CUDA-core
+ * kernel), 1 = always the token-serial kernel (a cross-check path). Errors:
+ * INVALID_ARGUMENT. */
+gdn_status gdn_set_kernel_preference(gdn_handle* handle, int32_t preference);
+
 /* Device workspace bytes that gdn_prefill_packed needs for this pack (the chunk/tile work
  * list). Validates the same arguments gdn_prefill_packed validates about the pack.
  * Result is a multiple of 256 and at least 256. */
@@ -140,6 +146,23 @@ gdn_status gdn_prefill_packed(gdn_handle* handle, const gdn_config* cfg, int32_t
                               const int32_t* ckpt_cu_host, const int32_t* ckpt_pos_host,
                               void* o, float* ckpt_states, float* final_states,
                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Host image of the work list that gdn_prefill_packed would upload for this pack and
+ * handle (handle may be NULL: automatic kernel choice), for inspection and tests. Layout,
+ * each array on a 256-byte boundary: int32 status, int32 num_units, then num_units units
+ * {int32 seq, head, row0, nrows} ordered longest prompt first, then per-prompt records
+ * {int32 tok_start, len, ckpt_begin, ckpt_end}, then the checkpoint positions.
+ * *bytes_needed receives the size; with out == NULL nothing else is written. Errors as
+ * gdn_prefill_packed's pack checks, or WORKSPACE_TOO_SMALL when out_bytes is short. */
+gdn_status gdn_prefill_worklist_host(gdn_handle* handle, const gdn_config* cfg,
+                                     int32_t num_seqs, const int32_t* cu_seqlens_host,
+                                     const int32_t* ckpt_cu_host, const int32_t* ckpt_pos_host,
+                                     void* out, size_t out_bytes, size_t* bytes_needed);
+
+/* Read the device status word that the last prefill using `workspace` left behind (0 when
+ * every bounded device-side wait completed, GDN_ERR_DEVICE_TIMEOUT when one gave up).
+ * Synchronises `stream`. Errors: INVALID_ARGUMENT, CUDA. */
+gdn_status gdn_read_device_status(const void* workspace, int32_t* status_out, void* stream);
 
 /* Copy `bytes` of device checkpoint states into the handle's pinned pool at byte offset
  * `pool_offset`, on the handle's side stream, after all work already queued on `stream`

@@ -1,0 +1,522 @@
+// gdn_api.cu — the C ABI: validation, the varlen work-list scheduler, launches, the
+// pinned snapshot pool and the side-stream checkpoint copy.
+//
+// Conventions (see include/gdn.h): every argument is checked on the host before anything
+// is enqueued ("reject unsupported combinations before model loading", pegainfer PR #786,
+// Changes); device work is asynchronous on the caller's stream; the handle owns only host
+// resources, a side stream and events, and destroying it drains that stream first.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/gdn.h"
+#include "gdn_internal.h"
+
+using gdn::GdnSeq;
+using gdn::GdnUnit;
+
+namespace {
+
+constexpr int kStagingSlots = 4;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct StagingSlot {
+  void* host = nullptr;   // pinned
+  size_t bytes = 0;
+  cudaEvent_t done = nullptr;  // recorded after the H2D copy out of this slot
+  bool used = false;
+};
+
+}  // namespace
+
+struct gdn_handle {
+  int device = 0;
+  void* pool = nullptr;
+  size_t pool_bytes = 0;
+  cudaStream_t side = nullptr;
+  cudaEvent_t compute_ready = nullptr;
+  cudaEvent_t copy_done = nullptr;
+  bool copy_pending = false;
+  StagingSlot slots[kStagingSlots];
+  int next_slot = 0;
+  int32_t kernel_pref = 0;
+};
+
+namespace {
+
+gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+// Work-list layout inside the workspace (each array on a 256-byte boundary):
+//   header {int32 status; int32 num_units;} | units | seqs | ckpt_pos
+struct ListLayout {
+  size_t units_off, seqs_off, pos_off, total;
+  int32_t num_units;
+};
+
+enum KernelFamily { kRecurrent = 1, kChunked = 2 };
+
+bool chunked_supported(const gdn_config* c) {
+  return c->io_dtype == GDN_BF16 && c->head_dim_k == 128 && c->head_dim_v == 128 &&
+         c->chunk_size == 64;
+}
+
+KernelFamily pick_kernel(const gdn_handle* h, const gdn_config* c) {
+  if (h && h->kernel_pref == 1) return kRecurrent;
+  if (gdn::kChunkedReady && chunked_supported(c)) return kChunked;
+  return kRecurrent;
+}
+
+int32_t units_per_head(KernelFamily f, int head_dim) {
+  return f == kRecurrent ? head_dim / gdn::kRecurrentRows : 1;
+}
+
+ListLayout layout_for(int32_t num_seqs, int32_t num_units, int32_t num_ckpt) {
+  ListLayout L;
+  L.num_units = num_units;
+  L.units_off = kAlign;
+  L.seqs_off = align_up(L.units_off + sizeof(GdnUnit) * (size_t)num_units, kAlign);
+  L.pos_off = align_up(L.seqs_off + sizeof(GdnSeq) * (size_t)num_seqs, kAlign);
+  L.total = align_up(L.pos_off + sizeof(int32_t) * (size_t)std::max(num_ckpt, 1), kAlign);
+  return L;
+}
+
+gdn_status check_config(const gdn_config* c) {
+  if (!c) return GDN_ERR_INVALID_ARGUMENT;
+  if (c->num_k_heads <= 0 || c->num_v_heads <= 0 || c->head_dim_k <= 0 || c->head_dim_v <= 0 ||
+      c->chunk_size <= 0)
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (c->num_v_heads % c->num_k_heads != 0) return GDN_ERR_INVALID_ARGUMENT;
+  if (c->io_dtype != GDN_F32 && c->io_dtype != GDN_BF16) return GDN_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(c->scale)) return GDN_ERR_INVALID_ARGUMENT;
+  if (c->head_dim_k != c->head_dim_v) return GDN_ERR_UNSUPPORTED;
+  if (c->head_dim_k != 64 && c->head_dim_k != 128) return GDN_ERR_UNSUPPORTED;
+  if (c->chunk_size != 64) return GDN_ERR_UNSUPPORTED;
+  return GDN_OK;
+}
+
+// Checks the pack description; fills *num_ckpt.
+gdn_status check_pack(const gdn_config* c, int32_t num_seqs, const int32_t* cu,
+                      const int32_t* ckpt_cu, const int32_t* ckpt_pos, int32_t* num_ckpt) {
+  if (num_seqs < 1 || !cu) return GDN_ERR_INVALID_ARGUMENT;
+  if (cu[0] != 0) return GDN_ERR_INVALID_ARGUMENT;
+  for (int32_t n = 0; n < num_seqs; ++n)
+    if (cu[n + 1] < cu[n]) return GDN_ERR_INVALID_ARGUMENT;
+  *num_ckpt = 0;
+  if (!ckpt_cu) return GDN_OK;
+  if (ckpt_cu[0] != 0) return GDN_ERR_INVALID_ARGUMENT;
+  for (int32_t n = 0; n < num_seqs; ++n)
+    if (ckpt_cu[n + 1] < ckpt_cu[n]) return GDN_ERR_INVALID_ARGUMENT;
+  const int32_t total = ckpt_cu[num_seqs];
+  if (total > 0 && !ckpt_pos) return GDN_ERR_INVALID_ARGUMENT;
+  gdn_status soft = GDN_OK;
+  for (int32_t n = 0; n < num_seqs; ++n) {
+    const int32_t len = cu[n + 1] - cu[n];
+    for (int32_t j = ckpt_cu[n]; j < ckpt_cu[n + 1]; ++j) {
+      const int32_t p = ckpt_pos[j];
+      if (p < 1 || p > len) return GDN_ERR_INVALID_ARGUMENT;
+      if (j > ckpt_cu[n] && p <= ckpt_pos[j - 1]) return GDN_ERR_INVALID_ARGUMENT;
+      if (p % c->chunk_size != 0 && p != len) soft = GDN_ERR_UNSUPPORTED;
+    }
+  }
+  *num_ckpt = total;
+  return soft;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;
+};
+bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// Fills the host image of the work list. Units: every (prompt, value head, row block),
+// ordered by prompt length, longest first (stable, so equal lengths keep pack order).
+void build_worklist(void* dst, const ListLayout& L, KernelFamily fam, const gdn_config* c,
+                    int32_t num_seqs, const int32_t* cu, const int32_t* ckpt_cu,
+                    const int32_t* ckpt_pos, int32_t num_ckpt) {
+  std::memset(dst, 0, L.total);
+  char* base = static_cast<char*>(dst);
+  int32_t* header = reinterpret_cast<int32_t*>(base);
+  header[0] = 0;  // device status word
+  header[1] = L.num_units;
+  GdnSeq* seqs = reinterpret_cast<GdnSeq*>(base + L.seqs_off);
+  for (int32_t n = 0; n < num_seqs; ++n) {
+    seqs[n].tok_start = cu[n];
+    seqs[n].len = cu[n + 1] - cu[n];
+    seqs[n].ckpt_begin = ckpt_cu ? ckpt_cu[n] : 0;
+    seqs[n].ckpt_end = ckpt_cu ? ckpt_cu[n + 1] : 0;
+  }
+  if (num_ckpt > 0)
+    std::memcpy(base + L.pos_off, ckpt_pos, sizeof(int32_t) * (size_t)num_ckpt);
+  std::vector<int32_t> order(num_seqs);
+  for (int32_t n = 0; n < num_seqs; ++n) order[n] = n;
+  std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) {
+    return (cu[x + 1] - cu[x]) > (cu[y + 1] - cu[y]);
+  });
+  GdnUnit* units = reinterpret_cast<GdnUnit*>(base + L.units_off);
+  const int32_t per_head = units_per_head(fam, c->head_dim_v);
+  const int32_t rows = c->head_dim_v / per_head;
+  int32_t u = 0;
+  for (int32_t n : order)
+    for (int32_t h = 0; h < c->num_v_heads; ++h)
+      for (int32_t r = 0; r < per_head; ++r) units[u++] = GdnUnit{n, h, r * rows, rows};
+}
+
+gdn_status plan(gdn_handle* h, const gdn_config* c, int32_t num_seqs, const int32_t* cu,
+                const int32_t* ckpt_cu, const int32_t* ckpt_pos, KernelFamily* fam,
+                ListLayout* L, int32_t* num_ckpt) {
+  gdn_status s = check_config(c);
+  if (s != GDN_OK) return s;
+  s = check_pack(c, num_seqs, cu, ckpt_cu, ckpt_pos, num_ckpt);
+  if (s != GDN_OK) return s;
+  *fam = pick_kernel(h, c);
+  const int64_t units =
+      (int64_t)num_seqs * c->num_v_heads * units_per_head(*fam, c->head_dim_v);
+  if (units > INT32_MAX) return GDN_ERR_UNSUPPORTED;
+  *L = layout_for(num_seqs, (int32_t)units, *num_ckpt);
+  return GDN_OK;
+}
+
+// Takes the next pinned staging slot, growing it if needed, after its previous copy.
+gdn_status take_slot(gdn_handle* h, size_t bytes, StagingSlot** out) {
+  StagingSlot& s = h->slots[h->next_slot];
+  h->next_slot = (h->next_slot + 1) % kStagingSlots;
+  if (s.used) {
+    if (cudaEventSynchronize(s.done) != cudaSuccess) return GDN_ERR_CUDA;
+  }
+  if (s.bytes < bytes) {
+    if (s.host) cudaFreeHost(s.host);
+    s.host = nullptr;
+    s.bytes = 0;
+    const size_t want = std::max(bytes, (size_t)1 << 16);
+    if (cudaHostAlloc(&s.host, want, cudaHostAllocDefault) != cudaSuccess) return GDN_ERR_CUDA;
+    s.bytes = want;
+  }
+  *out = &s;
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t gdn_abi_version(void) { return GDN_ABI_VERSION; }
+
+const char* gdn_status_string(int32_t s) {
+  switch (s) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case GDN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case GDN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case GDN_ERR_CUDA: return "CUDA error";
+    case GDN_ERR_DEVICE_TIMEOUT: return "device wait timed out or not finished";
+    case GDN_ERR_POOL_EXHAUSTED: return "range outside the pinned snapshot pool";
+    default: return "unknown status";
+  }
+}
+
+gdn_status gdn_handle_create(int32_t device, size_t pinned_pool_bytes, gdn_handle** out) {
+  if (!out) return GDN_ERR_INVALID_ARGUMENT;
+  *out = nullptr;
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess) return GDN_ERR_CUDA;
+  if (device < 0 || device >= count) return GDN_ERR_INVALID_ARGUMENT;
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (cudaSetDevice(device) != cudaSuccess) return GDN_ERR_CUDA;
+  gdn_handle* h = new (std::nothrow) gdn_handle();
+  if (!h) return GDN_ERR_CUDA;
+  h->device = device;
+  bool ok = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h->compute_ready, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h->copy_done, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; ok && i < kStagingSlots; ++i)
+    ok = cudaEventCreateWithFlags(&h->slots[i].done, cudaEventDisableTiming) == cudaSuccess;
+  if (ok && pinned_pool_bytes > 0) {
+    ok = cudaHostAlloc(&h->pool, pinned_pool_bytes, cudaHostAllocDefault) == cudaSuccess;
+    if (ok) h->pool_bytes = pinned_pool_bytes;
+  }
+  cudaSetDevice(prev);
+  if (!ok) {
+    gdn_handle_destroy(h);
+    return GDN_ERR_CUDA;
+  }
+  *out = h;
+  return GDN_OK;
+}
+
+gdn_status gdn_handle_destroy(gdn_handle* h) {
+  if (!h) return GDN_OK;
+  gdn_status st = GDN_OK;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(h->device);
+  if (h->side && cudaStreamSynchronize(h->side) != cudaSuccess) st = GDN_ERR_CUDA;
+  for (int i = 0; i < kStagingSlots; ++i) {
+    StagingSlot& s = h->slots[i];
+    if (s.used && s.done) cudaEventSynchronize(s.done);
+    if (s.done) cudaEventDestroy(s.done);
+    if (s.host) cudaFreeHost(s.host);
+  }
+  if (h->compute_ready) cudaEventDestroy(h->compute_ready);
+  if (h->copy_done) cudaEventDestroy(h->copy_done);
+  if (h->side) cudaStreamDestroy(h->side);
+  if (h->pool) cudaFreeHost(h->pool);
+  cudaSetDevice(prev);
+  delete h;
+  return st;
+}
+
+gdn_status gdn_pool_info(gdn_handle* h, void** host_ptr, size_t* bytes) {
+  if (!h || !host_ptr || !bytes) return GDN_ERR_INVALID_ARGUMENT;
+  *host_ptr = h->pool;
+  *bytes = h->pool_bytes;
+  return GDN_OK;
+}
+
+gdn_status gdn_set_kernel_preference(gdn_handle* h, int32_t pref) {
+  if (!h || pref < 0 || pref > 1) return GDN_ERR_INVALID_ARGUMENT;
+  h->kernel_pref = pref;
+  return GDN_OK;
+}
+
+gdn_status gdn_prefill_workspace_size(const gdn_config* cfg, int32_t num_seqs,
+                                      const int32_t* cu_seqlens_host,
+                                      const int32_t* ckpt_cu_host, size_t* bytes) {
+  if (!bytes) return GDN_ERR_INVALID_ARGUMENT;
+  gdn_status s = check_config(cfg);
+  if (s != GDN_OK) return s;
+  if (num_seqs < 1 || !cu_seqlens_host) return GDN_ERR_INVALID_ARGUMENT;
+  if (cu_seqlens_host[0] != 0) return GDN_ERR_INVALID_ARGUMENT;
+  for (int32_t n = 0; n < num_seqs; ++n)
+    if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return GDN_ERR_INVALID_ARGUMENT;
+  int32_t num_ckpt = 0;
+  if (ckpt_cu_host) {
+    if (ckpt_cu_host[0] != 0) return GDN_ERR_INVALID_ARGUMENT;
+    for (int32_t n = 0; n < num_seqs; ++n)
+      if (ckpt_cu_host[n + 1] < ckpt_cu_host[n]) return GDN_ERR_INVALID_ARGUMENT;
+    num_ckpt = ckpt_cu_host[num_seqs];
+  }
+  // sized for the family with the most units, so the answer does not depend on a handle
+  const int64_t units = (int64_t)num_seqs * cfg->num_v_heads *
+                        units_per_head(kRecurrent, cfg->head_dim_v);
+  if (units > INT32_MAX) return GDN_ERR_UNSUPPORTED;
+  *bytes = layout_for(num_seqs, (int32_t)units, num_ckpt).total;
+  return GDN_OK;
+}
+
+gdn_status gdn_prefill_packed(gdn_handle* h, const gdn_config* cfg, int32_t num_seqs,
+                              const int32_t* cu, const void* q, const void* k, const void* v,
+                              const float* a, const float* beta, const float* init,
+                              const int32_t* ckpt_cu, const int32_t* ckpt_pos, void* o,
+                              float* ckpt_states, float* final_states, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  KernelFamily fam;
+  ListLayout L;
+  int32_t num_ckpt = 0;
+  gdn_status s = plan(h, cfg, num_seqs, cu, ckpt_cu, ckpt_pos, &fam, &L, &num_ckpt);
+  if (s != GDN_OK) return s;
+  const int64_t T = cu[num_seqs];
+  const int D = cfg->head_dim_k;
+  const size_t es = cfg->io_dtype == GDN_BF16 ? 2 : 4;
+  if (T > 0 && (!q || !k || !v || !a || !beta || !o)) return GDN_ERR_INVALID_ARGUMENT;
+  if (!final_states) return GDN_ERR_INVALID_ARGUMENT;
+  if (num_ckpt > 0 && !ckpt_states) return GDN_ERR_INVALID_ARGUMENT;
+  const void* ptrs[] = {q, k, v, a, beta, init, o, ckpt_states, final_states};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return GDN_ERR_INVALID_ARGUMENT;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (workspace_bytes < L.total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+  if (!h) return GDN_ERR_INVALID_ARGUMENT;
+
+  // outputs must not overlap each other, the inputs or the workspace (final may == init)
+  const size_t state_bytes = (size_t)cfg->num_v_heads * D * D * 4;
+  auto rng = [](const void* p, size_t n) {
+    return Range{reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(p) + n};
+  };
+  const Range outs[] = {rng(o, (size_t)T * cfg->num_v_heads * D * es),
+                        rng(ckpt_states, (size_t)num_ckpt * state_bytes),
+                        rng(final_states, (size_t)num_seqs * state_bytes)};
+  const Range ins[] = {rng(q, (size_t)T * cfg->num_k_heads * D * es),
+                       rng(k, (size_t)T * cfg->num_k_heads * D * es),
+                       rng(v, (size_t)T * cfg->num_v_heads * D * es),
+                       rng(a, (size_t)T * cfg->num_v_heads * 4),
+                       rng(beta, (size_t)T * cfg->num_v_heads * 4),
+                       rng(workspace, L.total)};
+  for (int i = 0; i < 3; ++i) {
+    if (outs[i].lo == 0 || outs[i].hi == outs[i].lo) continue;
+    for (int j = i + 1; j < 3; ++j)
+      if (outs[j].lo && overlaps(outs[i], outs[j])) return GDN_ERR_INVALID_ARGUMENT;
+    for (const Range& r : ins)
+      if (r.lo && r.hi > r.lo && overlaps(outs[i], r)) return GDN_ERR_INVALID_ARGUMENT;
+  }
+  if (init && static_cast<const void*>(init) != static_cast<const void*>(final_states)) {
+    const Range ir = rng(init, (size_t)num_seqs * state_bytes);
+    for (const Range& r : outs)
+      if (r.lo && r.hi > r.lo && overlaps(ir, r)) return GDN_ERR_INVALID_ARGUMENT;
+  }
+
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (prev != h->device && cudaSetDevice(h->device) != cudaSuccess) return GDN_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  StagingSlot* slot = nullptr;
+  s = take_slot(h, L.total, &slot);
+  if (s == GDN_OK) {
+    build_worklist(slot->host, L, fam, cfg, num_seqs, cu, ckpt_cu, ckpt_pos, num_ckpt);
+    cudaError_t e = cudaMemcpyAsync(workspace, slot->host, L.total, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaEventRecord(slot->done, st);
+    slot->used = true;
+    if (e != cudaSuccess) s = GDN_ERR_CUDA;
+  }
+  if (s == GDN_OK) {
+    char* ws = static_cast<char*>(workspace);
+    gdn::PrefillArgs pa;
+    pa.q = q; pa.k = k; pa.v = v; pa.a = a; pa.beta = beta; pa.init = init;
+    pa.o = o; pa.ckpt = ckpt_states; pa.final_state = final_states;
+    pa.units = reinterpret_cast<const GdnUnit*>(ws + L.units_off);
+    pa.seqs = reinterpret_cast<const GdnSeq*>(ws + L.seqs_off);
+    pa.ckpt_pos = reinterpret_cast<const int32_t*>(ws + L.pos_off);
+    pa.num_units = L.num_units;
+    pa.hk_heads = cfg->num_k_heads;
+    pa.hv_heads = cfg->num_v_heads;
+    pa.group = cfg->num_v_heads / cfg->num_k_heads;
+    pa.scale = cfg->scale;
+    pa.l2norm = cfg->qk_l2norm ? 1 : 0;
+    pa.status = reinterpret_cast<int32_t*>(ws);
+    int e = fam == kChunked ? gdn::launch_chunked_prefill(pa, stream)
+                            : gdn::launch_recurrent_prefill(pa, D, cfg->io_dtype == GDN_BF16,
+                                                            stream);
+    if (e != 0) s = GDN_ERR_CUDA;
+  }
+  if (prev != h->device) cudaSetDevice(prev);
+  return s;
+}
+
+gdn_status gdn_prefill_worklist_host(gdn_handle* h, const gdn_config* cfg, int32_t num_seqs,
+                                     const int32_t* cu, const int32_t* ckpt_cu,
+                                     const int32_t* ckpt_pos, void* out, size_t out_bytes,
+                                     size_t* bytes_needed) {
+  KernelFamily fam;
+  ListLayout L;
+  int32_t num_ckpt = 0;
+  gdn_status s = plan(h, cfg, num_seqs, cu, ckpt_cu, ckpt_pos, &fam, &L, &num_ckpt);
+  if (s != GDN_OK) return s;
+  if (bytes_needed) *bytes_needed = L.total;
+  if (!out) return GDN_OK;
+  if (out_bytes < L.total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+  build_worklist(out, L, fam, cfg, num_seqs, cu, ckpt_cu, ckpt_pos, num_ckpt);
+  return GDN_OK;
+}
+
+gdn_status gdn_read_device_status(const void* workspace, int32_t* status_out, void* stream) {
+  if (!workspace || !status_out) return GDN_ERR_INVALID_ARGUMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GDN_ERR_CUDA;
+  *status_out = v;
+  return GDN_OK;
+}
+
+gdn_status gdn_checkpoint_copy(gdn_handle* h, const float* src, size_t bytes,
+                               size_t pool_offset, void* stream) {
+  if (!h || (!src && bytes > 0)) return GDN_ERR_INVALID_ARGUMENT;
+  if (pool_offset > h->pool_bytes || bytes > h->pool_bytes - pool_offset)
+    return GDN_ERR_POOL_EXHAUSTED;
+  if (bytes == 0) return GDN_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaEventRecord(h->compute_ready, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->compute_ready, 0);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(static_cast<char*>(h->pool) + pool_offset, src, bytes,
+                        cudaMemcpyDeviceToHost, h->side);
+  if (e == cudaSuccess) e = cudaEventRecord(h->copy_done, h->side);
+  if (e == cudaSuccess) h->copy_pending = true;
+  return cuda_status(e);
+}
+
+gdn_status gdn_checkpoint_copy_query(gdn_handle* h) {
+  if (!h) return GDN_ERR_INVALID_ARGUMENT;
+  if (!h->copy_pending) return GDN_OK;
+  cudaError_t e = cudaEventQuery(h->copy_done);
+  if (e == cudaSuccess) return GDN_OK;
+  if (e == cudaErrorNotReady) return GDN_ERR_DEVICE_TIMEOUT;
+  return GDN_ERR_CUDA;
+}
+
+gdn_status gdn_checkpoint_copy_wait(gdn_handle* h) {
+  if (!h) return GDN_ERR_INVALID_ARGUMENT;
+  if (!h->copy_pending) return GDN_OK;
+  return cuda_status(cudaEventSynchronize(h->copy_done));
+}
+
+gdn_status gdn_decode_step(gdn_handle* h, const gdn_config* cfg, int32_t batch, const void* q,
+                           const void* k, const void* v, const float* a, const float* beta,
+                           float* pool, int32_t num_slots, const int32_t* slot_idx, void* o,
+                           void* stream) {
+  gdn_status s = check_config(cfg);
+  if (s != GDN_OK) return s;
+  if (batch < 0 || num_slots < 0) return GDN_ERR_INVALID_ARGUMENT;
+  if (batch == 0) return GDN_OK;
+  if (!q || !k || !v || !a || !beta || !pool || !slot_idx || !o || num_slots < 1)
+    return GDN_ERR_INVALID_ARGUMENT;
+  const void* ptrs[] = {q, k, v, a, beta, pool, o};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return GDN_ERR_INVALID_ARGUMENT;
+  if ((int64_t)batch * cfg->num_v_heads * (cfg->head_dim_v / 32) > INT32_MAX)
+    return GDN_ERR_UNSUPPORTED;
+  if (!h) return GDN_ERR_INVALID_ARGUMENT;
+  gdn::DecodeArgs da;
+  da.q = q; da.k = k; da.v = v; da.a = a; da.beta = beta;
+  da.pool = pool; da.slot = slot_idx; da.o = o;
+  da.batch = batch;
+  da.hk_heads = cfg->num_k_heads;
+  da.hv_heads = cfg->num_v_heads;
+  da.group = cfg->num_v_heads / cfg->num_k_heads;
+  da.scale = cfg->scale;
+  da.l2norm = cfg->qk_l2norm ? 1 : 0;
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (prev != h->device && cudaSetDevice(h->device) != cudaSuccess) return GDN_ERR_CUDA;
+  int e = gdn::launch_decode(da, cfg->head_dim_k, cfg->io_dtype == GDN_BF16, stream);
+  if (prev != h->device) cudaSetDevice(prev);
+  return e == 0 ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int32_t gdn_ckpt_position(int32_t len, int32_t block, int32_t tail) {
+  if (len <= 0 || block <= 0 || tail < 0) return 0;
+  int32_t p = (len / block) * block;
+  if (p > len - tail) p -= block;
+  return p > 0 ? p : 0;
+}
+
+int32_t gdn_mixed_budget(int32_t num_waiting, const int32_t* remaining, int32_t budget,
+                         int32_t max_prompts, int32_t* take) {
+  if (num_waiting < 0 || budget < 0 || max_prompts < 0) return -1;
+  if (num_waiting > 0 && (!remaining || !take)) return -1;
+  int32_t left = budget, served = 0;
+  for (int32_t i = 0; i < num_waiting; ++i) {
+    take[i] = 0;
+    if (remaining[i] < 0) return -1;
+    if (i >= max_prompts || left <= 0) continue;
+    const int32_t t = std::min(remaining[i], left);
+    take[i] = t;
+    left -= t;
+    if (t > 0) ++served;
+  }
+  return served;
+}
+
+}  // extern "C"

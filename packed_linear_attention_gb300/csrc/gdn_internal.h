@@ -1,0 +1,83 @@
+// gdn_internal.h — structures shared by the C ABI layer and the CUDA kernels.
+//
+// The host scheduler turns cu_seqlens and the checkpoint CSR into a work list that is
+// uploaded once per call into the caller's workspace:
+//   [GdnUnit units[num_units]] [GdnSeq seqs[num_seqs]] [int32 ckpt_pos[num_ckpt]]
+// each array starting on a 256-byte boundary. A unit is one independent piece of the
+// recurrence: a (prompt, value head, block of state rows) triple. Rows of the state evolve
+// independently (row i only needs k, beta, g and row i itself), so a unit may own any row
+// block. Units are ordered longest prompt first so the hardware block scheduler, which
+// hands out blocks roughly in index order, runs a longest-processing-time-first schedule.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+namespace gdn {
+
+struct GdnUnit {
+  int32_t seq;    // prompt index in the pack
+  int32_t head;   // value head
+  int32_t row0;   // first state row (value dim) owned by the unit
+  int32_t nrows;  // number of rows
+};
+
+struct GdnSeq {
+  int32_t tok_start;   // cu_seqlens[n]
+  int32_t len;         // tokens in the prompt's segment
+  int32_t ckpt_begin;  // CSR range of this prompt's checkpoints
+  int32_t ckpt_end;
+};
+
+// Everything a prefill kernel needs besides the work list.
+struct PrefillArgs {
+  const void* q;          // [T][Hk][D]
+  const void* k;          // [T][Hk][D]
+  const void* v;          // [T][Hv][D]
+  const float* a;         // [T][Hv]
+  const float* beta;      // [T][Hv]
+  const float* init;      // [N][Hv][D][D] or nullptr
+  void* o;                // [T][Hv][D]
+  float* ckpt;            // [C][Hv][D][D]
+  float* final_state;     // [N][Hv][D][D]
+  const GdnUnit* units;
+  const GdnSeq* seqs;
+  const int32_t* ckpt_pos;
+  int32_t num_units;
+  int32_t hk_heads;
+  int32_t hv_heads;
+  int32_t group;          // Hv / Hk
+  float scale;
+  int32_t l2norm;
+  int32_t* status;        // device status word (0 = ok) or nullptr
+};
+
+struct DecodeArgs {
+  const void* q;          // [B][Hk][D]
+  const void* k;
+  const void* v;          // [B][Hv][D]
+  const float* a;         // [B][Hv]
+  const float* beta;
+  float* pool;            // [slots][Hv][D][D]
+  const int32_t* slot;    // [B]
+  void* o;                // [B][Hv][D]
+  int32_t batch;
+  int32_t hk_heads;
+  int32_t hv_heads;
+  int32_t group;
+  float scale;
+  int32_t l2norm;
+};
+
+constexpr float kL2NormEps = 1e-6f;
+
+// Launchers (defined in the .cu files). Return a cudaError_t as int.
+int launch_recurrent_prefill(const PrefillArgs& a, int head_dim, bool bf16, void* stream);
+int launch_decode(const DecodeArgs& a, int head_dim, bool bf16, void* stream);
+int launch_chunked_prefill(const PrefillArgs& a, void* stream);
+int chunked_prefill_smem_bytes();
+
+// Row block of a unit for each kernel family.
+constexpr int kRecurrentRows = 32;
+constexpr bool kChunkedReady = false;
+
+}  // namespace gdn

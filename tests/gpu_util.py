@@ -1,0 +1,94 @@
+"""Helpers shared by the GPU parity tests: run a pack through the C ABI, sample the
+oracle on whole (prompt, value head) units, and compare with the stated tolerances."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+from oracle import ref
+from packed_linear_attention_gb300 import gdn
+from packed_linear_attention_gb300 import inputs as I
+
+# bf16 io with fp32 state: rel-L2 <= 2e-3 and max-abs <= 1e-2 on o, every checkpoint and
+# every final state; fp32 io: <= 1e-4 for both.
+TOL = {"bf16": (2e-3, 1e-2), "f32": (1e-4, 1e-4)}
+
+
+def torch_cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch
+
+
+_handle = None
+
+
+def handle():
+    """One library handle per test process (with a 256 MiB pinned snapshot pool)."""
+    global _handle
+    if _handle is None:
+        from packed_linear_attention_gb300 import build
+        build.build()
+        _handle = gdn.gdn_handle_create(0, 256 << 20)
+    return _handle
+
+
+def run(pack, preference=gdn.KERNEL_AUTO, buf=None):
+    """Run gdn_prefill_packed on `pack`; returns (o, ckpt, final) as float64 NumPy arrays."""
+    torch = torch_cuda()
+    h = handle()
+    gdn.gdn_set_kernel_preference(h, preference)
+    try:
+        if buf is None:
+            buf = gdn.to_device(pack)
+        gdn.prefill(h, buf)
+        torch.cuda.synchronize()
+        assert gdn.gdn_read_device_status(buf.workspace) == 0
+    finally:
+        gdn.gdn_set_kernel_preference(h, gdn.KERNEL_AUTO)
+    return (buf.o.float().cpu().numpy().astype(np.float64),
+            buf.ckpt.cpu().numpy().astype(np.float64),
+            buf.final.cpu().numpy().astype(np.float64))
+
+
+def rel_l2(x, y):
+    den = np.linalg.norm(y)
+    return float(np.linalg.norm(x - y) / den) if den > 0 else float(np.linalg.norm(x))
+
+
+def assert_close(got, want, io_dtype, what=""):
+    rel_tol, abs_tol = TOL[io_dtype]
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    if want.size == 0:
+        return
+    r = rel_l2(got, want)
+    m = float(np.abs(got - want).max())
+    assert r <= rel_tol and m <= abs_tol, f"{what}: rel-L2 {r:.3e} max-abs {m:.3e}"
+
+
+def compare_units(pack, gpu, seqs, v_heads, per_item=True):
+    """Compare GPU results on chosen prompts and value heads with the oracle run on just
+    those units (units are independent, so the oracle's answer is the same as on the
+    whole pack)."""
+    o, ck, fin = gpu
+    sub = I.sub_pack(pack, seqs, v_heads)
+    ro, rck, rfin = ref.prefill(sub)
+    toks = np.concatenate([np.arange(pack.cu_seqlens[s], pack.cu_seqlens[s + 1])
+                           for s in seqs]).astype(np.int64)
+    heads = sub.meta["v_heads"]
+    go = o[toks][:, heads]
+    gck = np.concatenate([ck[pack.ckpt_cu[s]:pack.ckpt_cu[s + 1]] for s in seqs])[:, heads] \
+        if pack.num_ckpts else np.zeros((0,) + ck.shape[1:])[:, heads]
+    gfin = fin[seqs][:, heads]
+    assert_close(go, ro, pack.io_dtype, "o")
+    assert_close(gfin, rfin, pack.io_dtype, "final")
+    if rck.size:
+        assert_close(gck, rck, pack.io_dtype, "ckpt")
+    if per_item:
+        for j in range(rfin.shape[0]):
+            for hh in range(rfin.shape[1]):
+                assert_close(gfin[j, hh], rfin[j, hh], pack.io_dtype, f"final[{j},{hh}]")
+        for j in range(rck.shape[0]):
+            for hh in range(rck.shape[1]):
+                assert_close(gck[j, hh], rck[j, hh], pack.io_dtype, f"ckpt[{j},{hh}]")

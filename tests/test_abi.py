@@ -1,0 +1,151 @@
+"""The C ABI on the host: the library loads, exports every symbol the header declares,
+and rejects malformed calls before anything is launched (no GPU needed: validation comes
+before any CUDA call, and a NULL handle with well-formed arguments is itself an error)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from packed_linear_attention_gb300 import build, gdn
+from packed_linear_attention_gb300 import inputs as I
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return gdn.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(gdn.EXPORTS)
+
+
+def test_version_and_status_strings(lib):
+    assert gdn.gdn_abi_version() == 1
+    assert gdn.status_string(0) == "ok"
+    assert gdn.status_string(3) == "workspace too small"
+    assert gdn.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("length,expect", [(1024, 768), (1000, 768), (1030, 768),
+                                           (1040, 1024), (1039, 768), (270, 0), (0, 0)])
+def test_ckpt_position_rule(lib, length, expect):
+    assert gdn.gdn_ckpt_position(length, 256, 16) == expect
+    if length > 0:
+        assert I.ckpt_position_with_move_back(length, 256, 16) == expect
+
+
+def test_mixed_budget(lib):
+    assert gdn.gdn_mixed_budget([300, 500, 400, 100], 1024, 8) == (3, [300, 500, 224, 0])
+    assert gdn.gdn_mixed_budget([100] * 10, 1024, 8) == (8, [100] * 8 + [0, 0])
+    rng = np.random.default_rng(0)
+    for _ in range(50):
+        rem = rng.integers(1, 400, size=int(rng.integers(1, 12))).tolist()
+        served, take = gdn.gdn_mixed_budget(rem, 1024, 8)
+        assert take == I.mixed_budget(rem, 1024, 8)
+        assert sum(take) <= 1024 and served == sum(t > 0 for t in take)
+
+
+CFG = dict(num_k_heads=16, num_v_heads=32, head_dim=128)
+
+
+def _call(cfg=None, cu=(0, 100, 300), ckpt_cu=None, ckpt_pos=None, ptr=1 << 20, ws=1 << 20,
+          ws_bytes=None, handle=None, final=True, o=True):
+    cfg = cfg or gdn.make_config(**CFG)
+    if ws_bytes is None:
+        ws_bytes = 1 << 20
+    step = 1 << 28  # distinct, non-overlapping fake device ranges
+    P = lambda i: ptr + i * step
+    return gdn.gdn_prefill_packed(handle, cfg, list(cu), P(1), P(2), P(3), P(4), P(5), None,
+                                  ckpt_cu, ckpt_pos, P(6) if o else None, P(7),
+                                  P(8) if final else None, ws, ws_bytes, None,
+                                  raise_on_error=False)
+
+
+def test_prefill_validation(lib):
+    E = gdn
+    assert _call() == E.GDN_ERR_INVALID_ARGUMENT                        # NULL handle
+    assert _call(cu=(1, 100)) == E.GDN_ERR_INVALID_ARGUMENT              # cu[0] != 0
+    assert _call(cu=(0, 100, 50)) == E.GDN_ERR_INVALID_ARGUMENT          # decreasing
+    assert _call(cu=(0,)) == E.GDN_ERR_INVALID_ARGUMENT                  # no prompt
+    bad = gdn.make_config(**CFG)
+    bad.num_v_heads = 24
+    bad.num_k_heads = 16
+    assert _call(cfg=bad, ws_bytes=1 << 20) == E.GDN_ERR_INVALID_ARGUMENT  # Hv % Hk
+    bad = gdn.make_config(16, 32, 96)
+    assert _call(cfg=bad, ws_bytes=1 << 20) == E.GDN_ERR_UNSUPPORTED     # head dim
+    bad = gdn.make_config(16, 32, 128, chunk_size=32)
+    assert _call(cfg=bad, ws_bytes=1 << 20) == E.GDN_ERR_UNSUPPORTED     # chunk size
+    bad = gdn.make_config(16, 32, 128)
+    bad.io_dtype = 7
+    assert _call(cfg=bad, ws_bytes=1 << 20) == E.GDN_ERR_INVALID_ARGUMENT
+    # checkpoints: out of range, not increasing, off the chunk grid
+    assert _call(ckpt_cu=[0, 1, 1], ckpt_pos=[101]) == E.GDN_ERR_INVALID_ARGUMENT
+    assert _call(ckpt_cu=[0, 2, 2], ckpt_pos=[64, 64]) == E.GDN_ERR_INVALID_ARGUMENT
+    assert _call(ckpt_cu=[0, 1, 1], ckpt_pos=[50]) == E.GDN_ERR_UNSUPPORTED
+    # well-formed checkpoints (one at a prompt's end, one on the grid): only the NULL
+    # handle is left to complain about
+    assert _call(ckpt_cu=[0, 1, 2], ckpt_pos=[100, 128]) == E.GDN_ERR_INVALID_ARGUMENT
+    # workspace
+    assert _call(ws_bytes=255) == E.GDN_ERR_WORKSPACE_TOO_SMALL
+    assert _call(ws=(1 << 20) + 16) == E.GDN_ERR_INVALID_ARGUMENT          # misaligned
+    # missing outputs, misaligned input
+    assert _call(final=False) == E.GDN_ERR_INVALID_ARGUMENT
+    assert _call(o=False) == E.GDN_ERR_INVALID_ARGUMENT
+    assert _call(ptr=(1 << 20) + 8) == E.GDN_ERR_INVALID_ARGUMENT
+
+
+def test_prefill_rejects_overlapping_outputs(lib):
+    cfg = gdn.make_config(**CFG)
+    cu = [0, 64]
+    ws = gdn.gdn_prefill_workspace_size(cfg, cu)
+    base = 1 << 30
+    # o overlaps q
+    st = gdn.gdn_prefill_packed(None, cfg, cu, base, base + (1 << 24), base + (2 << 24),
+                                base + (3 << 24), base + (4 << 24), None, None, None,
+                                base + 4096, None, base + (5 << 24), base + (6 << 24), ws,
+                                None, raise_on_error=False)
+    assert st == gdn.GDN_ERR_INVALID_ARGUMENT
+
+
+def test_decode_validation(lib):
+    cfg = gdn.make_config(**CFG)
+    P = lambda i: (1 << 20) * (i + 1)
+    args = [P(1), P(2), P(3), P(4), P(5), P(6), 4, P(7), P(8)]
+    assert gdn.gdn_decode_step(None, cfg, 2, *args, raise_on_error=False) == \
+        gdn.GDN_ERR_INVALID_ARGUMENT                                       # NULL handle
+    assert gdn.gdn_decode_step(None, cfg, -1, *args, raise_on_error=False) == \
+        gdn.GDN_ERR_INVALID_ARGUMENT
+    bad = gdn.make_config(16, 32, 80)
+    assert gdn.gdn_decode_step(None, bad, 2, *args, raise_on_error=False) == \
+        gdn.GDN_ERR_UNSUPPORTED
+    args[0] = P(1) + 4
+    assert gdn.gdn_decode_step(None, cfg, 2, *args, raise_on_error=False) == \
+        gdn.GDN_ERR_INVALID_ARGUMENT
+
+
+def test_workspace_size_is_aligned_and_monotone(lib):
+    cfg = gdn.make_config(**CFG)
+    a = gdn.gdn_prefill_workspace_size(cfg, [0, 10])
+    b = gdn.gdn_prefill_workspace_size(cfg, [0, 10, 20, 30], [0, 0, 0, 1])
+    assert a % 256 == 0 and b % 256 == 0 and 256 <= a <= b
+
+
+def test_checkpoint_copy_bounds_without_pool(lib):
+    # NULL handle is an argument error; no CUDA call is made
+    assert lib.gdn_checkpoint_copy(None, ctypes.c_void_p(16), 16, 0, None) == \
+        gdn.GDN_ERR_INVALID_ARGUMENT

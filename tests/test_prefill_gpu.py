@@ -1,0 +1,201 @@
+"""GPU parity of gdn_prefill_packed against the fp64 oracle, through the C ABI.
+
+Workloads follow the serving pages: the 32 x 1,024 chat wave of sparkinfer v0.6.28
+(packed passes, one prefix-cache checkpoint per prompt moved back out of the last 16
+tokens), ragged prefix-cache hits resuming from stored states, 8K prompts, and the tiny
+fp32 pack. Packed-vs-alone identity is the pages' pack_ckpt_check, asserted bitwise.
+"""
+import numpy as np
+import pytest
+
+from oracle import ref
+from packed_linear_attention_gb300 import gdn
+from packed_linear_attention_gb300 import inputs as I
+
+from gpu_util import assert_close, compare_units, run, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = [gdn.KERNEL_AUTO, gdn.KERNEL_RECURRENT]
+
+
+@pytest.fixture(scope="module")
+def wave():
+    return I.chat_wave()
+
+
+@pytest.fixture(scope="module")
+def ragged():
+    return I.ragged_prefix()
+
+
+@pytest.mark.parametrize("pref", KERNELS)
+def test_tiny_f32_all_outputs(pref):
+    torch_cuda()
+    p = I.tiny_f32()
+    o, ck, fin = run(p, pref)
+    ro, rck, rfin = ref.prefill(p)
+    assert_close(o, ro, "f32", "o")
+    assert_close(ck, rck, "f32", "ckpt")
+    assert_close(fin, rfin, "f32", "final")
+    for j in range(rck.shape[0]):
+        assert_close(ck[j], rck[j], "f32", f"ckpt {j}")
+
+
+@pytest.mark.parametrize("pref", KERNELS)
+def test_tiny_dims_bf16(pref):
+    torch_cuda()
+    lengths = [17, 64, 100, 255]
+    p = I.make_pack(lengths, num_k_heads=2, num_v_heads=4, head_dim=64, io_dtype="bf16",
+                    seed=1, init_std=0.02, ckpt_lists=I.every_block(lengths, 64))
+    got = run(p, pref)
+    compare_units(p, got, list(range(4)), list(range(4)))
+
+
+@pytest.mark.parametrize("pref", KERNELS)
+def test_edge_lengths_d128(pref):
+    """Empty prompts, single tokens, chunk-1/chunk/chunk+1 tails, checkpoints at ends."""
+    torch_cuda()
+    lengths = [1, 2, 0, 63, 64, 65, 127, 128, 129, 200, 0, 3]
+    ck = [[p for p in range(64, n + 1, 64)] + ([n] if n % 64 and n > 0 else []) for n in lengths]
+    p = I.make_pack(lengths, num_k_heads=2, num_v_heads=4, head_dim=128, io_dtype="bf16",
+                    seed=2, init_std=0.02, ckpt_lists=ck)
+    got = run(p, pref)
+    compare_units(p, got, list(range(len(lengths))), list(range(4)))
+    # zero-length prompts: final state is the initial state, bit for bit
+    for n in (2, 10):
+        np.testing.assert_array_equal(got[2][n], p.init[n].astype(np.float64))
+
+
+def test_chat_wave_full_size_sampled(wave):
+    """The 32 x 1,024 wave at full size, in the bench's launch configuration; sampled
+    prompts and value heads (both members of two GQA groups) against the oracle."""
+    torch_cuda()
+    got = run(wave)
+    compare_units(wave, got, [0, 13, 31], [0, 1, 30, 31])
+
+
+def test_chat_wave_checkpoint_is_at_768(wave):
+    assert wave.ckpt_pos.tolist() == [768] * 32
+
+
+def test_ragged_prefix_full(ragged):
+    torch_cuda()
+    got = run(ragged)
+    compare_units(ragged, got, list(range(ragged.num_seqs)), [0, 1, 14, 15, 30, 31])
+
+
+def test_ragged_resume_from_checkpoint_equals_uninterrupted(ragged):
+    """Prefill to a checkpoint, resume from it: equal to the uninterrupted run (bitwise
+    when the cut is on the chunk grid, as every checkpoint here is)."""
+    torch = torch_cuda()
+    full = run(ragged)
+    # pick prompt 0 and its second checkpoint
+    n = 0
+    j0 = int(ragged.ckpt_cu[n])
+    cut = int(ragged.ckpt_pos[j0 + 1])
+    s, e = int(ragged.cu_seqlens[n]), int(ragged.cu_seqlens[n + 1])
+    rest = I.Pack(name="rest", cu_seqlens=np.array([0, e - s - cut], np.int32),
+                  q=ragged.q[s + cut:e], k=ragged.k[s + cut:e], v=ragged.v[s + cut:e],
+                  a=ragged.a[s + cut:e], beta=ragged.beta[s + cut:e],
+                  init=full[1][j0 + 1][None].astype(np.float32),
+                  ckpt_cu=np.zeros(2, np.int32), ckpt_pos=np.zeros(0, np.int32),
+                  num_k_heads=ragged.num_k_heads, num_v_heads=ragged.num_v_heads,
+                  head_dim=ragged.head_dim, io_dtype="bf16", scale=ragged.scale)
+    o2, _, fin2 = run(rest)
+    np.testing.assert_array_equal(o2, full[0][s + cut:e])
+    np.testing.assert_array_equal(fin2[0], full[2][n])
+
+
+def test_long_prompts_sampled():
+    torch_cuda()
+    p = I.long_prompts()
+    got = run(p)
+    compare_units(p, got, [1, 3], [2, 3, 20, 21])
+
+
+@pytest.mark.parametrize("pref", KERNELS)
+def test_pack_vs_alone_bitwise(pref):
+    """Each prompt alone and inside the pack: identical o, checkpoints and final state."""
+    torch_cuda()
+    lengths = [300, 64, 1, 1024, 0, 129, 700]
+    ck = [[q for q in range(64, n + 1, 64)] for n in lengths]
+    p = I.make_pack(lengths, num_k_heads=4, num_v_heads=8, head_dim=128, io_dtype="bf16",
+                    seed=4, init_std=0.02, ckpt_lists=ck)
+    o, c, f = run(p, pref)
+    for n in range(p.num_seqs):
+        s = I.sub_pack(p, [n])
+        o1, c1, f1 = run(s, pref)
+        np.testing.assert_array_equal(o[p.cu_seqlens[n]:p.cu_seqlens[n + 1]], o1)
+        np.testing.assert_array_equal(c[p.ckpt_cu[n]:p.ckpt_cu[n + 1]], c1)
+        np.testing.assert_array_equal(f[n], f1[0])
+
+
+@pytest.mark.parametrize("pref", KERNELS)
+def test_determinism(pref):
+    torch_cuda()
+    p = I.make_pack([500, 77, 1024], num_k_heads=4, num_v_heads=8, head_dim=128,
+                    io_dtype="bf16", seed=5, init_std=0.02, ckpt_lists=[[256], [], [512]])
+    a = run(p, pref)
+    b = run(p, pref)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_in_place_final_over_initial():
+    torch = torch_cuda()
+    p = I.make_pack([130, 64], num_k_heads=2, num_v_heads=4, head_dim=128, io_dtype="bf16",
+                    seed=6, init_std=0.02)
+    want = run(p)
+    buf = gdn.to_device(p)
+    buf.final = buf.init  # final_states aliases initial_state
+    from gpu_util import handle
+    gdn.prefill(handle(), buf)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(buf.init.cpu().numpy().astype(np.float64), want[2])
+
+
+def test_guard_bands_untouched():
+    """Outputs are written exactly inside their buffers: canaries around each survive."""
+    torch = torch_cuda()
+    from gpu_util import handle
+    lengths = [65, 1, 130]
+    p = I.make_pack(lengths, num_k_heads=2, num_v_heads=4, head_dim=128, io_dtype="bf16",
+                    seed=7, init_std=0.02, ckpt_lists=[[64, 65], [1], [128]])
+    buf = gdn.to_device(p)
+    G = 4096  # elements of guard on each side
+
+    def guarded(t):
+        big = torch.full((t.numel() + 2 * G,), float("nan"), dtype=t.dtype, device=t.device)
+        return big, big[G:G + t.numel()].view(t.shape)
+
+    o_big, buf.o = guarded(buf.o)
+    c_big, buf.ckpt = guarded(buf.ckpt)
+    f_big, buf.final = guarded(buf.final)
+    gdn.prefill(handle(), buf)
+    torch.cuda.synchronize()
+    for big in (o_big, c_big, f_big):
+        assert torch.isnan(big[:G].float()).all() and torch.isnan(big[-G:].float()).all()
+        assert not torch.isnan(big[G:-G].float()).any()
+
+
+def test_checkpoint_copy_to_pinned_pool(ragged):
+    """Checkpoints reach the handle's pinned pool through the side stream."""
+    torch = torch_cuda()
+    from gpu_util import handle
+    import ctypes
+    h = handle()
+    buf = gdn.to_device(ragged)
+    stream = torch.cuda.current_stream()
+    gdn.prefill(h, buf, stream)
+    nbytes = buf.ckpt.numel() * 4
+    offset = 4096
+    gdn.gdn_checkpoint_copy(h, buf.ckpt, nbytes, offset, stream)
+    gdn.gdn_checkpoint_copy_wait(h)
+    assert gdn.gdn_checkpoint_copy_query(h)
+    ptr, size = gdn.gdn_pool_info(h)
+    assert size >= nbytes + offset
+    host = np.ctypeslib.as_array((ctypes.c_float * (nbytes // 4)).from_address(ptr + offset))
+    np.testing.assert_array_equal(host.reshape(buf.ckpt.shape), buf.ckpt.cpu().numpy())
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_checkpoint_copy(h, buf.ckpt, size, 16, stream)
