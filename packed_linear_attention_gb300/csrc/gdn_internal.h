@@ -78,6 +78,6 @@ int chunked_prefill_smem_bytes();
 
 // Row block of a unit for each kernel family.
 constexpr int kRecurrentRows = 32;
-constexpr bool kChunkedReady = false;
+constexpr bool kChunkedReady = true;
 
 }  // namespace gdn
