@@ -195,6 +195,31 @@ gdn_status gdn_decode_step(gdn_handle* handle, const gdn_config* cfg, int32_t ba
                            float* state_pool, int32_t num_slots, const int32_t* slot_idx_dev,
                            void* o, void* stream);
 
+/* Bytes of the fixed device scratch behind gdn_prefill_packed_noalloc (per GPU). */
+#define GDN_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/* gdn_prefill_packed for callers that cannot allocate memory when they call in: there is
+ * no workspace and no handle argument, and nothing is allocated. The pages describe no
+ * such call; it exists for serving engines whose device memory is all handed to their own
+ * pool at start-up, and for plugins whose host framework forbids allocation on the request
+ * path. Arguments, layouts, results and errors are those of gdn_prefill_packed.
+ * The work list lives in one file-scope device array of GDN_NOALLOC_SCRATCH_BYTES per GPU
+ * (held from library load to process exit); a pack whose work list does not fit returns
+ * GDN_ERR_UNSUPPORTED before anything is enqueued. Every call rewrites that array and
+ * clears its status word, so calls whose device work may overlap in time (two streams)
+ * race and must be serialised by the caller. The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture. The host copy of the work list is taken from a
+ * fixed host buffer under a lock (pageable cudaMemcpyAsync). */
+gdn_status gdn_prefill_packed_noalloc(const gdn_config* cfg, int32_t num_seqs,
+                                      const int32_t* cu_seqlens_host,
+                                      const void* q, const void* k, const void* v,
+                                      const float* a, const float* beta,
+                                      const float* initial_state,
+                                      const int32_t* ckpt_cu_host, const int32_t* ckpt_pos_host,
+                                      void* o, float* ckpt_states, float* final_states,
+                                      void* stream);
+
 /* ---- host-side scheduling policy (no device work) ---------------------------------- */
 
 /* Prefix-cache checkpoint position of a prompt of `len` tokens on a grid of `block`

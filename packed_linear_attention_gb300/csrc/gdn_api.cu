@@ -520,3 +520,40 @@ int32_t gdn_mixed_budget(int32_t num_waiting, const int32_t* remaining, int32_t 
 }
 
 }  // extern "C"
+
+// ---- planning helpers for the allocation-free entry point (gdn_noalloc.cu) -------------
+
+namespace gdn {
+
+gdn_status plan_prefill(const gdn_handle* h, const gdn_config* cfg, int32_t num_seqs,
+                        const int32_t* cu, const int32_t* ckpt_cu, const int32_t* ckpt_pos,
+                        PrefillPlan* out) {
+  KernelFamily fam;
+  ListLayout L;
+  int32_t num_ckpt = 0;
+  gdn_status s = plan(const_cast<gdn_handle*>(h), cfg, num_seqs, cu, ckpt_cu, ckpt_pos, &fam,
+                      &L, &num_ckpt);
+  if (s != GDN_OK) return s;
+  out->family = fam;
+  out->units_off = L.units_off;
+  out->seqs_off = L.seqs_off;
+  out->pos_off = L.pos_off;
+  out->bytes = L.total;
+  out->num_units = L.num_units;
+  out->num_ckpt = num_ckpt;
+  return GDN_OK;
+}
+
+void write_worklist(void* dst, const PrefillPlan& plan, const gdn_config* cfg, int32_t num_seqs,
+                    const int32_t* cu, const int32_t* ckpt_cu, const int32_t* ckpt_pos) {
+  ListLayout L;
+  L.units_off = plan.units_off;
+  L.seqs_off = plan.seqs_off;
+  L.pos_off = plan.pos_off;
+  L.total = plan.bytes;
+  L.num_units = plan.num_units;
+  build_worklist(dst, L, static_cast<KernelFamily>(plan.family), cfg, num_seqs, cu, ckpt_cu,
+                 ckpt_pos, plan.num_ckpt);
+}
+
+}  // namespace gdn

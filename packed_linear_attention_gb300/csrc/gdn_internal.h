@@ -12,6 +12,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "../../include/gdn.h"
+
 namespace gdn {
 
 struct GdnUnit {
@@ -75,6 +77,19 @@ int launch_recurrent_prefill(const PrefillArgs& a, int head_dim, bool bf16, void
 int launch_decode(const DecodeArgs& a, int head_dim, bool bf16, void* stream);
 int launch_chunked_prefill(const PrefillArgs& a, void* stream);
 int chunked_prefill_smem_bytes();
+
+// Host-side planning shared with the allocation-free entry point (gdn_noalloc.cu):
+// the kernel family, the work-list layout and its size for one pack.
+struct PrefillPlan {
+  int family;            // 1 = token-serial, 2 = chunked tensor-core
+  size_t units_off, seqs_off, pos_off, bytes;
+  int32_t num_units, num_ckpt;
+};
+gdn_status plan_prefill(const gdn_handle* h, const gdn_config* cfg, int32_t num_seqs,
+                        const int32_t* cu, const int32_t* ckpt_cu, const int32_t* ckpt_pos,
+                        PrefillPlan* out);
+void write_worklist(void* dst, const PrefillPlan& plan, const gdn_config* cfg, int32_t num_seqs,
+                    const int32_t* cu, const int32_t* ckpt_cu, const int32_t* ckpt_pos);
 
 // Row block of a unit for each kernel family.
 constexpr int kRecurrentRows = 32;

@@ -37,6 +37,7 @@ EXPORTS = (
     "gdn_prefill_packed", "gdn_read_device_status", "gdn_checkpoint_copy",
     "gdn_checkpoint_copy_query", "gdn_checkpoint_copy_wait", "gdn_decode_step",
     "gdn_ckpt_position", "gdn_mixed_budget", "gdn_prefill_worklist_host",
+    "gdn_prefill_packed_noalloc",
 )
 
 
@@ -81,6 +82,8 @@ def load(path: str = LIB_PATH):
             "gdn_prefill_packed": (I32, [P, CFG, I32, IP, P, P, P, P, P, P, IP, IP, P, P, P,
                                          P, SZ, P]),
             "gdn_read_device_status": (I32, [P, IP, P]),
+            "gdn_prefill_packed_noalloc": (I32, [CFG, I32, IP, P, P, P, P, P, P, IP, IP, P, P,
+                                                 P, P]),
             "gdn_prefill_worklist_host": (I32, [P, CFG, I32, IP, IP, IP, P, SZ,
                                                 ctypes.POINTER(SZ)]),
             "gdn_checkpoint_copy": (I32, [P, P, SZ, SZ, P]),
@@ -185,6 +188,21 @@ def gdn_prefill_packed(handle, cfg, cu_seqlens, q, k, v, a, beta, initial_state,
         int(workspace_bytes), _stream(stream))
     if raise_on_error:
         _check(st, "gdn_prefill_packed")
+    return st
+
+
+def gdn_prefill_packed_noalloc(cfg, cu_seqlens, q, k, v, a, beta, initial_state, ckpt_cu,
+                               ckpt_pos, o, ckpt_states, final_states, stream=None, *,
+                               raise_on_error=True) -> int:
+    """gdn_prefill_packed without workspace or handle, for callers that cannot allocate at
+    call time; the work list goes to the library's fixed per-GPU device array."""
+    num_seqs = len(cu_seqlens) - 1
+    st = load().gdn_prefill_packed_noalloc(
+        ctypes.byref(cfg), num_seqs, _i32(cu_seqlens), _addr(q), _addr(k), _addr(v), _addr(a),
+        _addr(beta), _addr(initial_state), _i32(ckpt_cu), _i32(ckpt_pos), _addr(o),
+        _addr(ckpt_states), _addr(final_states), _stream(stream))
+    if raise_on_error:
+        _check(st, "gdn_prefill_packed_noalloc")
     return st
 
 
