@@ -394,7 +394,7 @@ gdn_status gdn_prefill_packed(gdn_handle* h, const gdn_config* cfg, int32_t num_
     pa.scale = cfg->scale;
     pa.l2norm = cfg->qk_l2norm ? 1 : 0;
     pa.status = reinterpret_cast<int32_t*>(ws);
-    int e = fam == kChunked ? gdn::launch_chunked_prefill(pa, stream)
+    int e = fam == kChunked ? gdn::launch_chunked_prefill(pa, T, stream)
                             : gdn::launch_recurrent_prefill(pa, D, cfg->io_dtype == GDN_BF16,
                                                             stream);
     if (e != 0) s = GDN_ERR_CUDA;

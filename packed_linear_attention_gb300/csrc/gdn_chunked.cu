@@ -8,29 +8,32 @@
 //     W^T   = K^T (T diag(beta e^G))^T            U^T = V^T (T diag(beta))^T
 //     D^T   = U^T - S W^T                          (row i of D: what token i writes)
 //     O^T   = S (diag(e^G) Q)^T + D^T P^T,         P_tj = exp(G_t - G_j) (q_t . k_j), j <= t
-//     S    <- e^{G_L} S + D^T diag(exp(G_L - G)) K
-// All exponents are <= 0. Every product runs on the tensor cores in the transposed
-// orientation, so the 128-row M side is always d_v or d_k and every MMA is M = 128.
+//     S    <- e^{G_L} S + (diag(exp(G_L - G)) D)^T K
+// All exponents are <= 0. Every tensor-core product runs in the transposed orientation, so
+// the 128-row M side is always d_v or d_k and every MMA is M = 128.
 //
-// Precision: every tensor-core operand is IEEE fp16 (11-bit significand) with fp32
-// accumulation; q and k are normalised in fp32 before their single rounding, v is widened
-// exactly from bf16, and the fp32 state is kept in TMEM (the fp16 copy that feeds the MMAs
-// is refreshed every chunk). This keeps outputs within 2e-3 relative L2 of an fp64
-// evaluation where bf16 operands would not. Operands must stay inside the fp16 range
-// (|v| and state entries below 65504).
+// Precision: every tcgen05 operand is IEEE fp16 (11-bit significand) with fp32
+// accumulation; q and k are normalised in fp32 before their rounding, v is widened exactly
+// from bf16, and the fp32 state lives in TMEM for the whole prompt (its fp16 copy feeds
+// the MMAs and is refreshed every chunk). The 64x64 triangular inverse is fp32 (diagonal
+// blocks by forward substitution, off-diagonal blocks by warp-level 3xTF32 products).
+// Operands must stay inside the fp16 range (|v| and state entries below 65504).
 //
-// Per CTA (256 threads, 8 warps): one unit, chunks in order. TMEM (256 columns):
-//   [0, 64)    R0: the current product (K K^T | Q K^T, W^T, D^T, O^T), fp32
-//   [64, 128)  S16: fp16 copy of S, the A operand of the state products
-//   [128, 256) S32: the fp32 state, accumulated in place by the update product
-// Shared memory holds the chunk's fp16 tiles in the 128B-swizzled layout (see
-// ptx_sm103.cuh), about 90 KB, so two CTAs share an SM and hide each other's latency.
+// Per CTA (256 threads, 8 warps, two CTAs per SM): one unit, chunks in order.
+//   TMEM (256 columns): [0,64) R0 = the current product (fp32); [64,128) S16 = fp16 state
+//   copy (A operand of the state products); [128,256) S32 = fp32 state, accumulated in
+//   place by the update product.
+//   Shared memory (128B-swizzled fp16 tiles, see ptx_sm103.cuh): raw bf16 q/k/v arrive by
+//   TMA and are converted in place; the next chunk's v is fetched as soon as the current
+//   one is consumed, q/k as soon as the last product of the chunk has read them.
 // Every mbarrier wait is bounded; a timeout is reported through the status word.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "gdn_internal.h"
 #include "ptx_sm103.cuh"
@@ -45,27 +48,33 @@ constexpr int kD = 128;         // head dim
 constexpr int kThreads = 256;
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr int kStatusTimeout = 5;  // GDN_ERR_DEVICE_TIMEOUT
-constexpr int kLd = 65;          // fp32 matrix row stride (bank-conflict padding)
+constexpr int kLd = 68;          // fp32 64x64 matrix row stride (conflict-free float4 rows)
+constexpr float kLog2e = 1.4426950408889634f;
 
 // shared-memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_KQ = 0;                       // [K;Q] 128 rows x 128 fp16: 32 KB
-constexpr uint32_t OFF_V = OFF_KQ + 32768;           // V: 64 rows x 128 fp16: 16 KB
-constexpr uint32_t OFF_P = OFF_V + 16384;            // P: 64 x 64 fp16: 8 KB
-constexpr uint32_t OFF_A = OFF_P + 8192;             // A fp32 [64][65], later T1 | T2 fp16
-constexpr uint32_t OFF_T1 = OFF_A;                   //   T diag(beta e^G): 8 KB
-constexpr uint32_t OFF_T2 = OFF_A + 8192;            //   T diag(beta): 8 KB
-constexpr uint32_t OFF_WD = OFF_A + 17408;           // T fp32 [64][65], then W^T, then D^T
-constexpr uint32_t OFF_X = OFF_WD + 17408;           // inverse scratch: 3 x 16 x 16 fp32
-constexpr uint32_t OFF_VEC = OFF_X + 3072;           // G, beta, 1/|k|, 1/|q|: 4 x 64 fp32
+constexpr uint32_t OFF_KQ = 0;         // K (rows 0-63) and Q (rows 64-127): 2 regions x 16 KB
+constexpr uint32_t OFF_V = 32768;      // V: 2 regions x 8 KB
+constexpr uint32_t OFF_P = 49152;      // P: 64 x 64 fp16
+constexpr uint32_t OFF_A = 57344;      // A fp32 [64][68] -> T1 | T2 -> D' -> o staging
+constexpr uint32_t OFF_T2 = OFF_A + 8192;
+constexpr uint32_t OFF_WD = 75776;     // T fp32 [64][68] -> W^T -> D
+constexpr uint32_t OFF_XS = OFF_WD + 17408;  // per-warp 16 x 8 fp32 scratch
+constexpr uint32_t OFF_VEC = OFF_XS + 4096;  // log2 gate sums, beta, decay factors
 constexpr uint32_t SMEM_USED = OFF_VEC + 1024;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;    // + alignment slack
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
 
 constexpr uint32_t TM_R0 = 0, TM_S16 = 64, TM_S32 = 128, TM_COLS = 256;
+constexpr uint32_t KQ_BYTES = 32768, V_BYTES = 16384;
+
+struct ChunkedParams {
+  PrefillArgs a;
+  CUtensorMap tq, tk, tv;  // 2D bf16 maps: (H*128 columns, T rows), 64 x 64 boxes, SW128
+};
 
 struct __align__(8) Smem {
-  uint64_t bar;
+  uint64_t bar_mma, bar_kq, bar_v;
   uint32_t tmem_base;
-  int32_t fail;
+  float next_decay;  // e^{G_L} of the next chunk
 };
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -73,17 +82,6 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Sum over the 16 lanes that share a token row.
-__device__ __forceinline__ float sum16(float x) {
-#pragma unroll
-  for (int off = 8; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-  return x;
-}
-
-// Stores 8 consecutive fp16 values (one 16-byte chunk) of tile row `row`, columns col..col+7.
 __device__ __forceinline__ void st_chunk(uint8_t* tile, uint32_t row, uint32_t col,
                                          uint32_t rows_per_region, const float (&x)[8]) {
   uint4 v;
@@ -95,25 +93,32 @@ __device__ __forceinline__ void st_chunk(uint8_t* tile, uint32_t row, uint32_t c
 }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4& w, float (&x)[8]) {
-  x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
-  x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
-}
-
-// Load this thread's 8-element slice of token row `t` (bf16) as fp32; zeros past the chunk.
-__device__ __forceinline__ void load_row8(const __nv_bfloat16* base, size_t row_stride, int t,
-                                          int L, int c8, float (&x)[8]) {
-  if (t < L) {
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(base + (size_t)t * row_stride + c8));
-    unpack_bf16x8(w, x);
-  } else {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = 0.f;
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(u[i] << 16);
+    x[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
   }
 }
 
-// Wait for the MMA barrier, uniformly across the block; returns false on timeout.
-__device__ __forceinline__ bool wait_mma(Smem& sm, uint32_t& phase) {
-  const bool ok = mbar_wait_bounded(&sm.bar, phase & 1u, kWaitLimit);
+__device__ __forceinline__ void unpack_half8(const uint4& w, float (&x)[8]) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+
+__device__ __forceinline__ uint4 pack_half8(const float (&x)[8]) {
+  return make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]),
+                    pack_half2(x[6], x[7]));
+}
+
+// Wait for an mbarrier phase, uniformly across the block; false on timeout.
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t& phase) {
+  const bool ok = mbar_wait_bounded(bar, phase & 1u, kWaitLimit);
   phase ^= 1u;
   tc_fence_after();
   return !__syncthreads_or(!ok);
@@ -127,13 +132,42 @@ __device__ __forceinline__ void publish_operands() {
   tc_fence_after();
 }
 
-// (I + A)^-1 for a 64 x 64 strictly-lower A (fp32, row stride kLd), by 16 x 16 blocks:
-// diagonal blocks by forward substitution, then T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj in
-// order of increasing i - j. Writes the lower triangle (with the unit diagonal) of T.
-__device__ void invert_unit_lower(const float* A, float* T, float* X, int tid) {
+// Issue the TMA loads of one chunk: q and k (4 boxes, one barrier) and/or v (2 boxes).
+__device__ __forceinline__ void issue_kq(const ChunkedParams& P, uint8_t* sKQ, uint64_t* bar,
+                                         int hk, int row) {
+  mbar_arrive_expect_tx(bar, KQ_BYTES);
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    tma_load_2d(sKQ + r * 16384, &P.tk, hk * kD + 64 * r, row, bar);
+    tma_load_2d(sKQ + r * 16384 + 8192, &P.tq, hk * kD + 64 * r, row, bar);
+  }
+}
+__device__ __forceinline__ void issue_v(const ChunkedParams& P, uint8_t* sV, uint64_t* bar,
+                                        int h, int row) {
+  mbar_arrive_expect_tx(bar, V_BYTES);
+  tma_load_2d(sV, &P.tv, h * kD, row, bar);
+  tma_load_2d(sV + 8192, &P.tv, h * kD + 64, row, bar);
+}
+
+// Loads the log-decays and betas of the chunk starting at token t0 (warp 0 only).
+__device__ __forceinline__ void load_gates(const float* ag, const float* bg, size_t stride,
+                                           int t0, int len, int lane, float (&g)[4]) {
+  const int L = min(kC, len - t0);
+  g[0] = lane < L ? __ldg(ag + (size_t)(t0 + lane) * stride) : 0.f;
+  g[1] = lane + 32 < L ? __ldg(ag + (size_t)(t0 + lane + 32) * stride) : 0.f;
+  g[2] = lane < L ? __ldg(bg + (size_t)(t0 + lane) * stride) : 0.f;
+  g[3] = lane + 32 < L ? __ldg(bg + (size_t)(t0 + lane + 32) * stride) : 0.f;
+}
+
+// (I + A)^-1 for a 64 x 64 strictly-lower A (fp32, row stride kLd) into T (same stride):
+// 16 x 16 diagonal blocks by forward substitution, then for block distance 1, 2, 3
+//     T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
+// with each 16 x 8 column slice of a block on one warp (3xTF32 warp MMAs). Only the lower
+// triangle and the unit diagonal of T are written.
+__device__ void invert_unit_lower(const float* A, float* T, float* xs, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
   if (warp < 4 && lane < 16) {
-    const int b = warp, j = lane, o = 16 * b;
+    const int o = 16 * warp, j = lane;
     float x[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -146,124 +180,148 @@ __device__ void invert_unit_lower(const float* A, float* T, float* X, int tid) {
     for (int i = 0; i < 16; ++i) T[(o + i) * kLd + o + j] = x[i];
   }
   __syncthreads();
-  // distance 1, 2, 3 between block row and block column
+  const int gid = lane >> 2, tig = lane & 3;
+  float* X = xs + warp * 128;  // 16 x 8, row stride 8
   for (int dist = 1; dist <= 3; ++dist) {
-    const int nblk = 4 - dist;  // blocks (bi, bj) with bi - bj = dist
-    for (int idx = tid; idx < nblk * 256; idx += kThreads) {
-      const int bj = idx >> 8, bi = bj + dist, r = (idx >> 4) & 15, c = idx & 15;
-      float s = 0.f;
-      for (int bk = bj; bk < bi; ++bk) {
-        const float* Ar = A + (16 * bi + r) * kLd + 16 * bk;
-        const float* Tc = T + (16 * bk) * kLd + 16 * bj + c;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) s += Ar[k] * Tc[k * kLd];
+    const int items = 2 * (4 - dist);
+    if (warp < items) {
+      const int bj = warp >> 1, bi = bj + dist;
+      const int r0 = 16 * bi, n0 = 16 * bj + 8 * (warp & 1);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int kk = 16 * bj; kk < 16 * bi; kk += 8) {
+        const float a[4] = {A[(r0 + gid) * kLd + kk + tig], A[(r0 + gid + 8) * kLd + kk + tig],
+                            A[(r0 + gid) * kLd + kk + tig + 4],
+                            A[(r0 + gid + 8) * kLd + kk + tig + 4]};
+        const float b[2] = {T[(kk + tig) * kLd + n0 + gid], T[(kk + tig + 4) * kLd + n0 + gid]};
+        mma_tf32x3(acc, a, b);
       }
-      X[idx] = s;
-    }
-    __syncthreads();
-    for (int idx = tid; idx < nblk * 256; idx += kThreads) {
-      const int bj = idx >> 8, bi = bj + dist, r = (idx >> 4) & 15, c = idx & 15;
-      const float* Tr = T + (16 * bi + r) * kLd + 16 * bi;
-      const float* Xc = X + (bj << 8) + c;
-      float s = 0.f;
+      X[gid * 8 + 2 * tig] = acc[0];
+      X[gid * 8 + 2 * tig + 1] = acc[1];
+      X[(gid + 8) * 8 + 2 * tig] = acc[2];
+      X[(gid + 8) * 8 + 2 * tig + 1] = acc[3];
+      __syncwarp();
+      float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int k = 0; k < 16; ++k) s += (k <= r ? Tr[k] : 0.f) * Xc[k * 16];
-      T[(16 * bi + r) * kLd + 16 * bj + c] = -s;
+      for (int k0 = 0; k0 < 16; k0 += 8) {
+        const float a[4] = {T[(r0 + gid) * kLd + r0 + k0 + tig],
+                            T[(r0 + gid + 8) * kLd + r0 + k0 + tig],
+                            T[(r0 + gid) * kLd + r0 + k0 + tig + 4],
+                            T[(r0 + gid + 8) * kLd + r0 + k0 + tig + 4]};
+        const float b[2] = {X[(k0 + tig) * 8 + gid], X[(k0 + tig + 4) * 8 + gid]};
+        mma_tf32x3(y, a, b);
+      }
+      T[(r0 + gid) * kLd + n0 + 2 * tig] = -y[0];
+      T[(r0 + gid) * kLd + n0 + 2 * tig + 1] = -y[1];
+      T[(r0 + gid + 8) * kLd + n0 + 2 * tig] = -y[2];
+      T[(r0 + gid + 8) * kLd + n0 + 2 * tig + 1] = -y[3];
     }
     __syncthreads();
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) chunked_prefill_kernel(PrefillArgs p) {
+__global__ void __launch_bounds__(kThreads, 2)
+chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Smem sm;
+  const PrefillArgs& p = P.a;
   uint8_t* sKQ = smem + OFF_KQ;
   uint8_t* sV = smem + OFF_V;
   uint8_t* sP = smem + OFF_P;
   float* sA = reinterpret_cast<float*>(smem + OFF_A);
-  uint8_t* sT1 = smem + OFF_T1;
+  uint8_t* sT1 = smem + OFF_A;
   uint8_t* sT2 = smem + OFF_T2;
+  uint8_t* sDp = smem + OFF_A;   // D' after the inverse and M3
+  uint8_t* sO = smem + OFF_A;    // bf16 output staging [64][128] after M5
   float* sT = reinterpret_cast<float*>(smem + OFF_WD);
   uint8_t* sWD = smem + OFF_WD;
-  float* sX = reinterpret_cast<float*>(smem + OFF_X);
-  float* sG = reinterpret_cast<float*>(smem + OFF_VEC);
+  float* sXs = reinterpret_cast<float*>(smem + OFF_XS);
+  float* sG = reinterpret_cast<float*>(smem + OFF_VEC);  // log2-scaled cumulative log-decay
   float* sB = sG + 64;
-  float* sRk = sG + 128;
-  float* sRq = sG + 192;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const GdnUnit u = p.units[blockIdx.x];
   const GdnSeq sd = p.seqs[u.seq];
   const int h = u.head, hk = h / p.group;
-  const size_t qk_stride = (size_t)p.hk_heads * kD;  // elements between tokens
   const size_t v_stride = (size_t)p.hv_heads * kD;
-  const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q) +
-                            (size_t)sd.tok_start * qk_stride + (size_t)hk * kD;
-  const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(p.k) +
-                            (size_t)sd.tok_start * qk_stride + (size_t)hk * kD;
-  const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(p.v) +
-                            (size_t)sd.tok_start * v_stride + (size_t)h * kD;
   __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.o) + (size_t)sd.tok_start * v_stride +
                       (size_t)h * kD;
   const float* ag = p.a + (size_t)sd.tok_start * p.hv_heads + h;
   const float* bg = p.beta + (size_t)sd.tok_start * p.hv_heads + h;
   const size_t state_off = ((size_t)u.seq * p.hv_heads + h) * kD * kD;
+  const int nchunks = (sd.len + kC - 1) / kC;
 
   if (tid == 0) {
-    mbar_init(&sm.bar, 1);
+    mbar_init(&sm.bar_mma, 1);
+    mbar_init(&sm.bar_kq, 1);
+    mbar_init(&sm.bar_v, 1);
     fence_mbar_init();
-    sm.fail = 0;
+    fence_proxy_async_smem();
+    if (nchunks > 0) {
+      prefetch_tmap(&P.tq);
+      prefetch_tmap(&P.tk);
+      prefetch_tmap(&P.tv);
+      issue_kq(P, sKQ, &sm.bar_kq, hk, sd.tok_start);
+      issue_v(P, sV, &sm.bar_v, h, sd.tok_start);
+    }
   }
   if (warp == 0) {
     tmem_alloc(&sm.tmem_base, TM_COLS);
     tmem_relinquish();
   }
+  // gates of chunk 0 (warp 0 keeps the next chunk's gates in registers)
+  float gnext[4] = {0.f, 0.f, 0.f, 0.f};
+  if (warp == 0 && nchunks > 0) {
+    load_gates(ag, bg, p.hv_heads, 0, sd.len, lane, gnext);
+    float s = gnext[0] + gnext[1];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) sm.next_decay = __expf(s);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
-  // this warp's TMEM lanes (subpartition) and column half
   const uint32_t sub = warp & 3, half = warp >> 2;
-  const uint32_t row = 32 * sub + lane;             // TMEM lane = matrix row of this thread
+  const uint32_t row = 32 * sub + lane;  // TMEM lane = matrix row of this thread
   const uint32_t t_lane = tbase + ((32 * sub) << 16);
 
-  // ---- initial state -> S32 (fp32) and S16 (fp16) -----------------------------------
+  // ---- initial state -> S32 (scaled by the first chunk's decay) and S16 ----------------
   {
+    const float d0 = nchunks > 0 ? sm.next_decay : 1.f;
     const float* src = p.init ? p.init + state_off + (size_t)row * kD + 64 * half : nullptr;
 #pragma unroll
     for (int c0 = 0; c0 < 64; c0 += 16) {
-      uint32_t r[16];
+      uint32_t r[16], h8[8];
 #pragma unroll
       for (int e = 0; e < 16; e += 4) {
-        float4 v = src ? __ldg(reinterpret_cast<const float4*>(src + c0 + e))
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-        r[e] = __float_as_uint(v.x); r[e + 1] = __float_as_uint(v.y);
-        r[e + 2] = __float_as_uint(v.z); r[e + 3] = __float_as_uint(v.w);
+        const float4 v = src ? __ldg(reinterpret_cast<const float4*>(src + c0 + e))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        r[e] = __float_as_uint(v.x * d0); r[e + 1] = __float_as_uint(v.y * d0);
+        r[e + 2] = __float_as_uint(v.z * d0); r[e + 3] = __float_as_uint(v.w * d0);
+        h8[e / 2] = pack_half2(v.x, v.y);
+        h8[e / 2 + 1] = pack_half2(v.z, v.w);
       }
       tmem_st16(t_lane + TM_S32 + 64 * half + c0, r);
-      uint32_t h8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        h8[e] = pack_half2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
       tmem_st8(t_lane + TM_S16 + 32 * half + c0 / 2, h8);
     }
     tmem_st_wait();
   }
 
-  uint32_t phase = 0;
+  uint32_t ph_mma = 0, ph_kq = 0, ph_v = 0;
   bool ok = true;
+  bool kq_inflight = nchunks > 0, v_inflight = nchunks > 0;  // meaningful in thread 0
   int c_next = sd.ckpt_begin;
   const float scale = p.scale;
 
-  for (int t0 = 0; t0 < sd.len && ok; t0 += kC) {
+  for (int c = 0; c < nchunks && ok; ++c) {
+    const int t0 = c * kC;
     const int L = min(kC, sd.len - t0);
 
-    // ---- (1) gates: G = chunk-local inclusive cumsum of a; beta (zero past L) ----------
+    // ---- (1) gates of this chunk from registers; fetch the next chunk's ------------------
     if (warp == 0) {
-      float a0 = lane < L ? __ldg(ag + (size_t)(t0 + lane) * p.hv_heads) : 0.f;
-      float a1 = lane + 32 < L ? __ldg(ag + (size_t)(t0 + lane + 32) * p.hv_heads) : 0.f;
+      float a0 = gnext[0] * kLog2e, a1 = gnext[1] * kLog2e;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const float y0 = __shfl_up_sync(0xffffffffu, a0, off);
@@ -273,38 +331,59 @@ __global__ void __launch_bounds__(kThreads, 2) chunked_prefill_kernel(PrefillArg
       a1 += __shfl_sync(0xffffffffu, a0, 31);
       sG[lane] = a0;
       sG[lane + 32] = a1;
-      sB[lane] = lane < L ? __ldg(bg + (size_t)(t0 + lane) * p.hv_heads) : 0.f;
-      sB[lane + 32] = lane + 32 < L ? __ldg(bg + (size_t)(t0 + lane + 32) * p.hv_heads) : 0.f;
+      sB[lane] = gnext[2];
+      sB[lane + 32] = gnext[3];
+      if (c + 1 < nchunks) {
+        load_gates(ag, bg, p.hv_heads, t0 + kC, sd.len, lane, gnext);
+        float s = gnext[0] + gnext[1];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (lane == 0) sm.next_decay = __expf(s);
+      }
     }
 
-    // ---- (2) normalised K (rows 0-63) and Q (rows 64-127), V, all fp16 -------------------
+    // ---- (2) wait for q, k, v; convert in place to fp16 (q, k normalised); zero past L ----
+    if (!(ok = wait_all(&sm.bar_kq, ph_kq))) break;
+    kq_inflight = false;
+    if (!(ok = wait_all(&sm.bar_v, ph_v))) break;
+    v_inflight = false;
     {
-      const int rsub = tid >> 4, c8 = (tid & 15) * 8;  // 16 rows per pass, 8 cols/thread
+      const int j = tid & 15, rsub = tid >> 4;  // 16 threads per row, chunk j of the row
+      const uint32_t reg = j >> 3, cc = j & 7;
+#pragma unroll 2
+      for (int pass = 0; pass < 8; ++pass) {   // K rows 0-63, Q rows 64-127
+        const uint32_t r = pass * 16 + rsub, t = r & 63;
+        uint4* ptr = reinterpret_cast<uint4*>(sKQ + reg * 16384 + (r >> 3) * 1024 +
+                                              (r & 7) * 128 + ((cc ^ (r & 7)) << 4));
+        float x[8];
+        unpack_bf16x8(*ptr, x);
+        float ss = 0.f;
 #pragma unroll
-      for (int pass = 0; pass < 4; ++pass) {
-        const int t = pass * 16 + rsub;
-        float xk[8], xq[8], xv[8];
-        load_row8(kg + (size_t)t0 * qk_stride, qk_stride, t, L, c8, xk);
-        load_row8(qg + (size_t)t0 * qk_stride, qk_stride, t, L, c8, xq);
-        load_row8(vg + (size_t)t0 * v_stride, v_stride, t, L, c8, xv);
-        float kk = 0.f, qq = 0.f;
+        for (int e = 0; e < 8; ++e) ss += x[e] * x[e];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) { kk += xk[e] * xk[e]; qq += xq[e] * xq[e]; }
-        kk = sum16(kk);
-        qq = sum16(qq);
-        const float rk = p.l2norm ? rsqrtf(kk + kL2NormEps) : 1.f;
-        const float rq = p.l2norm ? rsqrtf(qq + kL2NormEps) : 1.f;
+        for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float rn = (int)t < L ? (p.l2norm ? rsqrtf(ss + kL2NormEps) : 1.f) : 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) { xk[e] *= rk; xq[e] *= rq; }
-        st_chunk(sKQ, t, c8, 128, xk);
-        st_chunk(sKQ, 64 + t, c8, 128, xq);
-        st_chunk(sV, t, c8, 64, xv);
-        if ((tid & 15) == 0) { sRk[t] = rk; sRq[t] = rq; }
+        for (int e = 0; e < 8; ++e) x[e] *= rn;
+        *ptr = pack_half8(x);
+      }
+#pragma unroll 2
+      for (int pass = 0; pass < 4; ++pass) {   // V rows 0-63
+        const uint32_t r = pass * 16 + rsub;
+        uint4* ptr = reinterpret_cast<uint4*>(sV + reg * 8192 + (r >> 3) * 1024 +
+                                              (r & 7) * 128 + ((cc ^ (r & 7)) << 4));
+        float x[8];
+        unpack_bf16x8(*ptr, x);
+        if ((int)r >= L) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        }
+        *ptr = pack_half8(x);
       }
     }
     publish_operands();
 
-    // ---- (3) M1: [K; Q] K^T -> R0 (128 x 64) ------------------------------------------
+    // ---- (3) M1: [K; Q] K^T -> R0 (128 x 64) ------------------------------------------------
     if (tid == 0) {
       const uint32_t idesc = idesc_f16(128, 64, 0, 0);
       const uint32_t a0 = smem_u32(sKQ);
@@ -314,12 +393,12 @@ __global__ void __launch_bounds__(kThreads, 2) chunked_prefill_kernel(PrefillArg
         mma_f16_ss(tbase + TM_R0, smem_desc_sw128(a0 + off, 16, 1024),
                    smem_desc_sw128(a0 + off, 16, 1024), idesc, s > 0);
       }
-      mma_commit(&sm.bar);
+      mma_commit(&sm.bar_mma);
     }
     __syncwarp();
-    if (!(ok = wait_mma(sm, phase))) break;
+    if (!(ok = wait_all(&sm.bar_mma, ph_mma))) break;
 
-    // ---- (4) A (rows 0-63) and P (rows 64-127) from R0 ------------------------------------
+    // ---- (4) A (rows 0-63, fp32) and P (rows 64-127, fp16) from R0; Q~ = e^G Q over Q -----
     {
       uint32_t r[32];
       tmem_ld32(t_lane + TM_R0 + 32 * half, r);
@@ -329,9 +408,15 @@ __global__ void __launch_bounds__(kThreads, 2) chunked_prefill_kernel(PrefillArg
         const int i = row;
         const float gi = sG[i], bi = sB[i];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int j = j0 + e;
-          sA[i * kLd + j] = j < i ? bi * __expf(gi - sG[j]) * __uint_as_float(r[e]) : 0.f;
+        for (int e = 0; e < 32; e += 4) {
+          float4 v;
+          float* vv = reinterpret_cast<float*>(&v);
+#pragma unroll
+          for (int f = 0; f < 4; ++f) {
+            const int j = j0 + e + f;
+            vv[f] = j < i ? bi * exp2f(gi - sG[j]) * __uint_as_float(r[e + f]) : 0.f;
+          }
+          *reinterpret_cast<float4*>(sA + i * kLd + j0 + e) = v;
         }
       } else {
         const int t = row - 64;
@@ -342,29 +427,43 @@ __global__ void __launch_bounds__(kThreads, 2) chunked_prefill_kernel(PrefillArg
 #pragma unroll
           for (int f = 0; f < 8; ++f) {
             const int j = j0 + e + f;
-            x[f] = j <= t ? __expf(gt - sG[j]) * __uint_as_float(r[e + f]) : 0.f;
+            x[f] = j <= t ? exp2f(gt - sG[j]) * __uint_as_float(r[e + f]) : 0.f;
           }
           st_chunk(sP, t, j0 + e, 64, x);
         }
+      }
+      // Q~ rows: Q row t scaled by e^{G_t} (M1 has consumed Q)
+      const int j = tid & 15, rsub = tid >> 4;
+      const uint32_t reg = j >> 3, cc = j & 7;
+#pragma unroll
+      for (int pass = 0; pass < 4; ++pass) {
+        const uint32_t t = pass * 16 + rsub, rr = 64 + t;
+        uint4* ptr = reinterpret_cast<uint4*>(sKQ + reg * 16384 + (rr >> 3) * 1024 +
+                                              (rr & 7) * 128 + ((cc ^ (rr & 7)) << 4));
+        float x[8];
+        unpack_half8(*ptr, x);
+        const float gm = exp2f(sG[t]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] *= gm;
+        *ptr = pack_half8(x);
       }
     }
     tc_fence_before();
     __syncthreads();
 
-    // ---- (5) T = (I + A)^-1; T1 = T diag(beta e^G), T2 = T diag(beta) in fp16 ---------------
-    invert_unit_lower(sA, sT, sX, tid);
+    // ---- (5) T = (I + A)^-1; T1 = T diag(beta e^G), T2 = T diag(beta) (fp16) -----------------
+    invert_unit_lower(sA, sT, sXs, tid);
     {
       const int i = tid >> 2, jb = (tid & 3) * 16;
-      float x1[8], x2[8];
 #pragma unroll
       for (int h8 = 0; h8 < 16; h8 += 8) {
+        float x1[8], x2[8];
 #pragma unroll
         for (int f = 0; f < 8; ++f) {
           const int j = jb + h8 + f;
           const float tij = j <= i ? sT[i * kLd + j] : 0.f;
-          const float bj = sB[j];
-          x2[f] = tij * bj;
-          x1[f] = x2[f] * __expf(sG[j]);
+          x2[f] = tij * sB[j];
+          x1[f] = x2[f] * exp2f(sG[j]);
         }
         st_chunk(sT1, i, jb + h8, 64, x1);
         st_chunk(sT2, i, jb + h8, 64, x2);
@@ -372,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 2) chunked_prefill_kernel(PrefillArg
     }
     publish_operands();
 
-    // ---- (6) M2: W^T = K^T T1^T -> R0 (128 x 64) -------------------------------------------
+    // ---- (6) M2: W^T = K^T T1^T -> R0 (128 x 64) -----------------------------------------------
     if (tid == 0) {
       const uint32_t idesc = idesc_f16(128, 64, 1, 0);
       const uint32_t a0 = smem_u32(sKQ), b0 = smem_u32(sT1);
@@ -380,75 +479,12 @@ __global__ void __launch_bounds__(kThreads, 2) chunked_prefill_kernel(PrefillArg
       for (int s = 0; s < kC / 16; ++s)
         mma_f16_ss(tbase + TM_R0, smem_desc_sw128(a0 + s * 2048, 16384, 1024),
                    smem_desc_sw128(b0 + s * 32, 16, 1024), idesc, s > 0);
-      mma_commit(&sm.bar);
+      mma_commit(&sm.bar_mma);
     }
     __syncwarp();
-    if (!(ok = wait_mma(sm, phase))) break;
+    if (!(ok = wait_all(&sm.bar_mma, ph_mma))) break;
 
-    // ---- (7) W^T -> smem (fp16); K~, Q~ over K, Q; S32 *= e^{G_L} ----------------------------
-    {
-      uint32_t r[32];
-      tmem_ld32(t_lane + TM_R0 + 32 * half, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int e = 0; e < 32; e += 8) {
-        float x[8];
-#pragma unroll
-        for (int f = 0; f < 8; ++f) x[f] = __uint_as_float(r[e + f]);
-        st_chunk(sWD, row, 32 * half + e, 128, x);  // W^T row d_k, columns = tokens
-      }
-      const float gL = sG[L - 1];
-      const float decay = __expf(gL);
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t s32[32];
-        tmem_ld32(t_lane + TM_S32 + 64 * half + c0, s32);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) s32[e] = __float_as_uint(__uint_as_float(s32[e]) * decay);
-        uint32_t lo[16], hi[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) { lo[e] = s32[e]; hi[e] = s32[16 + e]; }
-        tmem_st16(t_lane + TM_S32 + 64 * half + c0, lo);
-        tmem_st16(t_lane + TM_S32 + 64 * half + c0 + 16, hi);
-      }
-      const int rsub = tid >> 4, c8 = (tid & 15) * 8;
-#pragma unroll
-      for (int pass = 0; pass < 4; ++pass) {
-        const int t = pass * 16 + rsub;
-        float xk[8], xq[8];
-        load_row8(kg + (size_t)t0 * qk_stride, qk_stride, t, L, c8, xk);
-        load_row8(qg + (size_t)t0 * qk_stride, qk_stride, t, L, c8, xq);
-        const float fk = sRk[t] * __expf(gL - sG[t]);
-        const float fq = sRq[t] * __expf(sG[t]);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) { xk[e] *= fk; xq[e] *= fq; }
-        st_chunk(sKQ, t, c8, 128, xk);
-        st_chunk(sKQ, 64 + t, c8, 128, xq);
-      }
-      tmem_st_wait();
-    }
-    publish_operands();
-
-    // ---- (8) M3: D^T = V^T T2^T - S16 W^T -> R0 -------------------------------------------------
-    if (tid == 0) {
-      const uint32_t id_u = idesc_f16(128, 64, 1, 0);
-      const uint32_t id_w = idesc_f16(128, 64, 0, 1, 0, 1);  // B negated
-      const uint32_t v0 = smem_u32(sV), t2 = smem_u32(sT2), w0 = smem_u32(sWD);
-#pragma unroll
-      for (int s = 0; s < kC / 16; ++s)
-        mma_f16_ss(tbase + TM_R0, smem_desc_sw128(v0 + s * 2048, 8192, 1024),
-                   smem_desc_sw128(t2 + s * 32, 16, 1024), id_u, s > 0);
-#pragma unroll
-      for (int s = 0; s < kD / 16; ++s)
-        mma_f16_ts(tbase + TM_R0, tbase + TM_S16 + s * 8,
-                   smem_desc_sw128(w0 + s * 2048, 16384, 1024), id_w, 1);
-      mma_commit(&sm.bar);
-    }
-    __syncwarp();
-    if (!(ok = wait_mma(sm, phase))) break;
-
-    // ---- (9) D^T -> smem (fp16, K-major A: rows d_v, columns tokens) ------------------------
+    // ---- (7) W^T -> smem (fp16, MN-major B: rows d_k, columns tokens) ---------------------------
     {
       uint32_t r[32];
       tmem_ld32(t_lane + TM_R0 + 32 * half, r);
@@ -463,11 +499,55 @@ __global__ void __launch_bounds__(kThreads, 2) chunked_prefill_kernel(PrefillArg
     }
     publish_operands();
 
-    // ---- (10) M4/M5: O^T = S16 Q~^T + D^T P^T -> R0; S32 += D^T K~ ----------------------------
+    // ---- (8) M3: D^T = V^T T2^T - S16 W^T -> R0 ------------------------------------------------
+    if (tid == 0) {
+      const uint32_t id_u = idesc_f16(128, 64, 1, 0);
+      const uint32_t id_w = idesc_f16(128, 64, 0, 1, 0, 1);  // B negated
+      const uint32_t v0 = smem_u32(sV), t2 = smem_u32(sT2), w0 = smem_u32(sWD);
+#pragma unroll
+      for (int s = 0; s < kC / 16; ++s)
+        mma_f16_ss(tbase + TM_R0, smem_desc_sw128(v0 + s * 2048, 8192, 1024),
+                   smem_desc_sw128(t2 + s * 32, 16, 1024), id_u, s > 0);
+#pragma unroll
+      for (int s = 0; s < kD / 16; ++s)
+        mma_f16_ts(tbase + TM_R0, tbase + TM_S16 + s * 8,
+                   smem_desc_sw128(w0 + s * 2048, 16384, 1024), id_w, 1);
+      mma_commit(&sm.bar_mma);
+    }
+    __syncwarp();
+    if (!(ok = wait_all(&sm.bar_mma, ph_mma))) break;
+    // V and T2 are consumed: fetch the next chunk's v now
+    if (tid == 0 && c + 1 < nchunks) {
+      issue_v(P, sV, &sm.bar_v, h, sd.tok_start + t0 + kC);
+      v_inflight = true;
+    }
+
+    // ---- (9) D^T and D'^T = D^T diag(e^{G_L - G}) -> smem (fp16 K-major A operands) -------------
+    {
+      uint32_t r[32];
+      tmem_ld32(t_lane + TM_R0 + 32 * half, r);
+      tmem_ld_wait();
+      const float gL = sG[L - 1];
+#pragma unroll
+      for (int e = 0; e < 32; e += 8) {
+        float x[8], y[8];
+#pragma unroll
+        for (int f = 0; f < 8; ++f) {
+          x[f] = __uint_as_float(r[e + f]);
+          y[f] = x[f] * exp2f(gL - sG[32 * half + e + f]);
+        }
+        st_chunk(sWD, row, 32 * half + e, 128, x);
+        st_chunk(sDp, row, 32 * half + e, 128, y);
+      }
+    }
+    publish_operands();
+
+    // ---- (10) O^T = S16 Q~^T + D^T P^T -> R0;  S32 += D'^T K ----------------------------------
     if (tid == 0) {
       const uint32_t id_n64 = idesc_f16(128, 64, 0, 0);
       const uint32_t id_n128 = idesc_f16(128, 128, 0, 1);
-      const uint32_t kq = smem_u32(sKQ), d0 = smem_u32(sWD), p0 = smem_u32(sP);
+      const uint32_t kq = smem_u32(sKQ), d0 = smem_u32(sWD), dp = smem_u32(sDp),
+                     p0 = smem_u32(sP);
 #pragma unroll
       for (int s = 0; s < kD / 16; ++s) {
         const uint32_t off = 8192 + (s >> 2) * 16384 + (s & 3) * 32;  // Q~ rows 64-127
@@ -480,27 +560,32 @@ __global__ void __launch_bounds__(kThreads, 2) chunked_prefill_kernel(PrefillArg
                    smem_desc_sw128(p0 + s * 32, 16, 1024), id_n64, 1);
 #pragma unroll
       for (int s = 0; s < kC / 16; ++s)
-        mma_f16_ss(tbase + TM_S32, smem_desc_sw128(d0 + s * 32, 16, 1024),
+        mma_f16_ss(tbase + TM_S32, smem_desc_sw128(dp + s * 32, 16, 1024),
                    smem_desc_sw128(kq + s * 2048, 16384, 1024), id_n128, 1);
-      mma_commit(&sm.bar);
+      mma_commit(&sm.bar_mma);
     }
     __syncwarp();
-    if (!(ok = wait_mma(sm, phase))) break;
+    if (!(ok = wait_all(&sm.bar_mma, ph_mma))) break;
+    // q and k are consumed: fetch the next chunk's
+    if (tid == 0 && c + 1 < nchunks) {
+      issue_kq(P, sKQ, &sm.bar_kq, hk, sd.tok_start + t0 + kC);
+      kq_inflight = true;
+    }
 
-    // ---- (11) o, S16 refresh, checkpoints ---------------------------------------------------
+    // ---- (11) o via smem staging; S16 refresh; checkpoints; pre-scale S32 for the next chunk --
     {
       uint32_t r[32];
       tmem_ld32(t_lane + TM_R0 + 32 * half, r);
       tmem_ld_wait();
+      __nv_bfloat16* so = reinterpret_cast<__nv_bfloat16*>(sO);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int t = 32 * half + e;
-        if (t < L)
-          og[(size_t)(t0 + t) * v_stride + row] = __float2bfloat16_rn(scale * __uint_as_float(r[e]));
-      }
+      for (int e = 0; e < 32; ++e)
+        so[(32 * half + e) * kD + row] = __float2bfloat16_rn(scale * __uint_as_float(r[e]));
+
       const int pos = t0 + L;
       const bool emit = c_next < sd.ckpt_end && p.ckpt_pos[c_next] == pos;
-      const bool last = pos == sd.len;
+      const bool last = c + 1 == nchunks;
+      const float nd = last ? 1.f : sm.next_decay;
       float* ck = emit ? p.ckpt + ((size_t)c_next * p.hv_heads + h) * kD * kD + (size_t)row * kD
                        : nullptr;
       float* fin = last ? p.final_state + state_off + (size_t)row * kD : nullptr;
@@ -526,10 +611,28 @@ __global__ void __launch_bounds__(kThreads, 2) chunked_prefill_kernel(PrefillArg
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<uint4*>(fin + col + e) =
                 make_uint4(s32[e], s32[e + 1], s32[e + 2], s32[e + 3]);
+        } else {
+          uint32_t lo[16], hi[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            lo[e] = __float_as_uint(__uint_as_float(s32[e]) * nd);
+            hi[e] = __float_as_uint(__uint_as_float(s32[16 + e]) * nd);
+          }
+          tmem_st16(t_lane + TM_S32 + 64 * half + c0, lo);
+          tmem_st16(t_lane + TM_S32 + 64 * half + c0 + 16, hi);
         }
       }
       if (emit) ++c_next;
       tmem_st_wait();
+      __syncthreads();
+      // coalesced 16-byte stores of the chunk's output rows
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int idx = it * kThreads + tid, t = idx >> 4, ch = idx & 15;
+        if (t < L)
+          *reinterpret_cast<uint4*>(og + (size_t)(t0 + t) * v_stride + ch * 8) =
+              *reinterpret_cast<const uint4*>(sO + t * 256 + ch * 16);
+      }
     }
     tc_fence_before();
     __syncthreads();
@@ -546,19 +649,61 @@ __global__ void __launch_bounds__(kThreads, 2) chunked_prefill_kernel(PrefillArg
   }
   if (!ok) {
     if (tid == 0 && p.status) atomicExch(p.status, kStatusTimeout);
-    // give an MMA that may still be in flight one more bounded chance to land
-    mbar_wait_bounded(&sm.bar, phase & 1u, kWaitLimit);
+    // let products and copies still in flight land (bounded) before TMEM and shared
+    // memory are released: the MMA barrier's pending phase is the one that timed out
+    // (or was never waited), and thread 0 knows which tensor copies are outstanding
+    if (tid == 0) {
+      mbar_wait_bounded(&sm.bar_mma, ph_mma & 1u, kWaitLimit);
+      if (kq_inflight) mbar_wait_bounded(&sm.bar_kq, ph_kq & 1u, kWaitLimit);
+      if (v_inflight) mbar_wait_bounded(&sm.bar_v, ph_v & 1u, kWaitLimit);
+    }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tbase, TM_COLS);
 }
 
+// ---- host: tensor maps ------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 2D map over a [rows][cols] bf16 matrix (row stride = cols), 64 x 64 boxes, 128B swizzle;
+// reads past the last row return zeros.
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 }  // namespace
 
 int chunked_prefill_smem_bytes() { return (int)SMEM_BYTES; }
 
-int launch_chunked_prefill(const PrefillArgs& a, void* stream) {
+int launch_chunked_prefill(const PrefillArgs& a, int64_t total_tokens, void* stream) {
   if (a.num_units == 0) return 0;
   static bool configured = false;
   if (!configured) {
@@ -568,7 +713,20 @@ int launch_chunked_prefill(const PrefillArgs& a, void* stream) {
     if (e != cudaSuccess) return (int)e;
     configured = true;
   }
-  chunked_prefill_kernel<<<a.num_units, kThreads, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(a);
+  ChunkedParams P;
+  P.a = a;
+  const uint64_t rows = total_tokens > 0 ? (uint64_t)total_tokens : 1;
+  if (total_tokens > 0) {
+    if (!make_map(&P.tq, a.q, (uint64_t)a.hk_heads * kD, rows) ||
+        !make_map(&P.tk, a.k, (uint64_t)a.hk_heads * kD, rows) ||
+        !make_map(&P.tv, a.v, (uint64_t)a.hv_heads * kD, rows))
+      return (int)cudaErrorInvalidValue;
+  } else {
+    memset(&P.tq, 0, sizeof(CUtensorMap));
+    memset(&P.tk, 0, sizeof(CUtensorMap));
+    memset(&P.tv, 0, sizeof(CUtensorMap));
+  }
+  chunked_prefill_kernel<<<a.num_units, kThreads, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(P);
   return (int)cudaGetLastError();
 }
 

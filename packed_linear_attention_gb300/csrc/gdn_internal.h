@@ -75,7 +75,7 @@ constexpr float kL2NormEps = 1e-6f;
 // Launchers (defined in the .cu files). Return a cudaError_t as int.
 int launch_recurrent_prefill(const PrefillArgs& a, int head_dim, bool bf16, void* stream);
 int launch_decode(const DecodeArgs& a, int head_dim, bool bf16, void* stream);
-int launch_chunked_prefill(const PrefillArgs& a, void* stream);
+int launch_chunked_prefill(const PrefillArgs& a, int64_t total_tokens, void* stream);
 int chunked_prefill_smem_bytes();
 
 // Host-side planning shared with the allocation-free entry point (gdn_noalloc.cu):

@@ -119,7 +119,7 @@ extern "C" gdn_status gdn_prefill_packed_noalloc(const gdn_config* cfg, int32_t 
   pa.l2norm = cfg->qk_l2norm ? 1 : 0;
   pa.status = reinterpret_cast<int32_t*>(scratch);
   const int e = plan.family == 2
-                    ? gdn::launch_chunked_prefill(pa, stream)
+                    ? gdn::launch_chunked_prefill(pa, T, stream)
                     : gdn::launch_recurrent_prefill(pa, D, cfg->io_dtype == GDN_BF16, stream);
   return e == 0 ? GDN_OK : GDN_ERR_CUDA;
 }
