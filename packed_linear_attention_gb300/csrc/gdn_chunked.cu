@@ -58,9 +58,9 @@ constexpr uint32_t OFF_P = 49152;      // P: 64 x 64 fp16
 constexpr uint32_t OFF_A = 57344;      // A fp32 [64][68] -> T1 | T2 -> D' -> o staging
 constexpr uint32_t OFF_T2 = OFF_A + 8192;
 constexpr uint32_t OFF_WD = 75776;     // T fp32 [64][68] -> W^T -> D
-constexpr uint32_t OFF_XS = OFF_WD + 17408;  // per-warp 16 x 8 fp32 scratch
-constexpr uint32_t OFF_VEC = OFF_XS + 4096;  // log2 gate sums, beta, decay factors
-constexpr uint32_t SMEM_USED = OFF_VEC + 1024;
+constexpr uint32_t OFF_XS = OFF_WD + 17408;  // inverse scratch: 32 x 36 fp32
+constexpr uint32_t OFF_VEC = OFF_XS + 5120;  // per-token gate factors: 5 x 64 fp32
+constexpr uint32_t SMEM_USED = OFF_VEC + 2048;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
 
 constexpr uint32_t TM_R0 = 0, TM_S16 = 64, TM_S32 = 128, TM_COLS = 256;
@@ -111,6 +111,19 @@ __device__ __forceinline__ void unpack_half8(const uint4& w, float (&x)[8]) {
   }
 }
 
+// bf16 -> fp16 is exact for magnitudes in [2^-17, 65504] (8 significant bits fit in 11).
+__device__ __forceinline__ uint4 bf16x8_to_half8(const uint4& w) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 hh = __floats2half2_rn(__uint_as_float(u[i] << 16),
+                                         __uint_as_float(u[i] & 0xFFFF0000u));
+    o[i] = *reinterpret_cast<const uint32_t*>(&hh);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 __device__ __forceinline__ uint4 pack_half8(const float (&x)[8]) {
   return make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]),
                     pack_half2(x[6], x[7]));
@@ -159,64 +172,90 @@ __device__ __forceinline__ void load_gates(const float* ag, const float* bg, siz
   g[3] = lane + 32 < L ? __ldg(bg + (size_t)(t0 + lane + 32) * stride) : 0.f;
 }
 
+// One 16 x 8 output tile D = sum_k Ablk[r0.., k] * Bblk[k.., n0..] over k in [k_lo, k_hi)
+// (multiples of 8) on one warp, tf32 warp MMAs. Both matrices fp32 with row strides lda/ldb.
+__device__ __forceinline__ void tile_mm(float (&d)[4], const float* Am, int lda, int r0,
+                                        const float* Bm, int ldb, int n0, int k_lo, int k_hi,
+                                        int gid, int tig) {
+  for (int k = k_lo; k < k_hi; k += 8) {
+    const float a[4] = {Am[(r0 + gid) * lda + k + tig], Am[(r0 + gid + 8) * lda + k + tig],
+                        Am[(r0 + gid) * lda + k + tig + 4], Am[(r0 + gid + 8) * lda + k + tig + 4]};
+    const float b[2] = {Bm[(k + tig) * ldb + n0 + gid], Bm[(k + tig + 4) * ldb + n0 + gid]};
+    mma_tf32_f(d, a, b);
+  }
+}
+
+// Stores a 16 x 8 accumulator tile (optionally negated) at (r0, n0) of an fp32 matrix.
+__device__ __forceinline__ void tile_store(float* M, int ld, int r0, int n0, const float (&d)[4],
+                                           float sign, int gid, int tig) {
+  M[(r0 + gid) * ld + n0 + 2 * tig] = sign * d[0];
+  M[(r0 + gid) * ld + n0 + 2 * tig + 1] = sign * d[1];
+  M[(r0 + gid + 8) * ld + n0 + 2 * tig] = sign * d[2];
+  M[(r0 + gid + 8) * ld + n0 + 2 * tig + 1] = sign * d[3];
+}
+
+constexpr int kLdX = 36;  // row stride of the 32 x 32 merge scratch
+
 // (I + A)^-1 for a 64 x 64 strictly-lower A (fp32, row stride kLd) into T (same stride):
-// 16 x 16 diagonal blocks by forward substitution, then for block distance 1, 2, 3
-//     T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
-// with each 16 x 8 column slice of a block on one warp (3xTF32 warp MMAs). Only the lower
-// triangle and the unit diagonal of T are written.
-__device__ void invert_unit_lower(const float* A, float* T, float* xs, int tid) {
+//  1. (invert_diag_blocks) the four 16 x 16 diagonal blocks by right-looking forward
+//     substitution in fp32 (two blocks per warp, one column per lane);
+//  2. (invert_merge) recursive doubling: for L = [[L11, 0], [L21, L22]], L^-1 has off-diagonal block
+//     -L22^-1 L21 L11^-1; first for the 16 x 16 pairs, then for the two 32 x 32 halves.
+// Products run on tf32 warp MMAs: the off-diagonal blocks are small next to the unit
+// diagonal, so their tf32 rounding leaves T within about 1e-6 relative, far below the fp16
+// rounding of the operands built from T. Only the lower triangle and the unit diagonal of
+// T are written; blocks of T above the diagonal are never read.
+// Step 1 of the inverse, run by warps 0 and 1 while the other warps do independent work.
+__device__ __forceinline__ void invert_diag_blocks(const float* A, float* T, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
-  if (warp < 4 && lane < 16) {
-    const int o = 16 * warp, j = lane;
-    float x[16];
+  const int o = 16 * (2 * warp + (lane >> 4)), j = lane & 15;
+  float x[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float s = 0.f;
+  for (int i = 0; i < 16; ++i) x[i] = i == j ? 1.f : 0.f;
 #pragma unroll
-      for (int k = 0; k < i; ++k) s += A[(o + i) * kLd + o + k] * x[k];
-      x[i] = (i == j) ? 1.f : (i < j ? 0.f : -s);
-    }
+  for (int k = 0; k < 15; ++k) {
+    const float xk = x[k];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) T[(o + i) * kLd + o + j] = x[i];
+    for (int i = k + 1; i < 16; ++i) x[i] -= A[(o + i) * kLd + o + k] * xk;
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) T[(o + i) * kLd + o + j] = x[i];
+}
+
+// Step 2 of the inverse (all warps), after the diagonal blocks are in T.
+__device__ void invert_merge(const float* A, float* T, float* X, int tid) {
+  const int warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
+  // 16 -> 32: T[16b+16.., 16b..] = -T22 (A21 T11) for b = 0, 2; warps 0-3, one 8-column slice
+  if (warp < 4) {
+    const int b = 2 * (warp >> 1), r0 = 16 * b + 16, n0 = 16 * b + 8 * (warp & 1);
+    float* xs = X + warp * 128;  // 16 x 8 scratch, row stride 8
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    tile_mm(d, A, kLd, r0, T, kLd, n0, 16 * b, 16 * b + 16, gid, tig);
+    tile_store(xs, 8, 0, 0, d, 1.f, gid, tig);
+    __syncwarp();
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+    tile_mm(y, T + r0 * kLd + r0, kLd, 0, xs, 8, 0, 0, 16, gid, tig);
+    tile_store(T, kLd, r0, n0, y, -1.f, gid, tig);
   }
   __syncthreads();
-  const int gid = lane >> 2, tig = lane & 3;
-  float* X = xs + warp * 128;  // 16 x 8, row stride 8
-  for (int dist = 1; dist <= 3; ++dist) {
-    const int items = 2 * (4 - dist);
-    if (warp < items) {
-      const int bj = warp >> 1, bi = bj + dist;
-      const int r0 = 16 * bi, n0 = 16 * bj + 8 * (warp & 1);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int kk = 16 * bj; kk < 16 * bi; kk += 8) {
-        const float a[4] = {A[(r0 + gid) * kLd + kk + tig], A[(r0 + gid + 8) * kLd + kk + tig],
-                            A[(r0 + gid) * kLd + kk + tig + 4],
-                            A[(r0 + gid + 8) * kLd + kk + tig + 4]};
-        const float b[2] = {T[(kk + tig) * kLd + n0 + gid], T[(kk + tig + 4) * kLd + n0 + gid]};
-        mma_tf32x3(acc, a, b);
-      }
-      X[gid * 8 + 2 * tig] = acc[0];
-      X[gid * 8 + 2 * tig + 1] = acc[1];
-      X[(gid + 8) * 8 + 2 * tig] = acc[2];
-      X[(gid + 8) * 8 + 2 * tig + 1] = acc[3];
-      __syncwarp();
-      float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int k0 = 0; k0 < 16; k0 += 8) {
-        const float a[4] = {T[(r0 + gid) * kLd + r0 + k0 + tig],
-                            T[(r0 + gid + 8) * kLd + r0 + k0 + tig],
-                            T[(r0 + gid) * kLd + r0 + k0 + tig + 4],
-                            T[(r0 + gid + 8) * kLd + r0 + k0 + tig + 4]};
-        const float b[2] = {X[(k0 + tig) * 8 + gid], X[(k0 + tig + 4) * 8 + gid]};
-        mma_tf32x3(y, a, b);
-      }
-      T[(r0 + gid) * kLd + n0 + 2 * tig] = -y[0];
-      T[(r0 + gid) * kLd + n0 + 2 * tig + 1] = -y[1];
-      T[(r0 + gid + 8) * kLd + n0 + 2 * tig] = -y[2];
-      T[(r0 + gid + 8) * kLd + n0 + 2 * tig + 1] = -y[3];
-    }
-    __syncthreads();
+  // 32 -> 64: X = A[32:64, 0:32] T[0:32, 0:32], then T[32:64, 0:32] = -T[32:64, 32:64] X;
+  // eight 16 x 8 tiles, one per warp; zero blocks of the triangular factors are skipped
+  {
+    const int mt = warp >> 2, nt = warp & 3;
+    const int r0 = 16 * mt, n0 = 8 * nt;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    tile_mm(d, A + 32 * kLd, kLd, r0, T, kLd, n0, nt >= 2 ? 16 : 0, 32, gid, tig);
+    tile_store(X, kLdX, r0, n0, d, 1.f, gid, tig);
   }
+  __syncthreads();
+  {
+    const int mt = warp >> 2, nt = warp & 3;
+    const int r0 = 16 * mt, n0 = 8 * nt;
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+    tile_mm(y, T + 32 * kLd + 32, kLd, r0, X, kLdX, n0, 0, mt == 0 ? 16 : 32, gid, tig);
+    tile_store(T, kLd, 32 + r0, n0, y, -1.f, gid, tig);
+  }
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
@@ -238,7 +277,13 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
   uint8_t* sWD = smem + OFF_WD;
   float* sXs = reinterpret_cast<float*>(smem + OFF_XS);
   float* sG = reinterpret_cast<float*>(smem + OFF_VEC);  // log2-scaled cumulative log-decay
-  float* sB = sG + 64;
+  float* sB = sG + 64;     // beta
+  float* sGq = sG + 128;   // scale e^{G_t} / |q_t|: row factor of Q~
+  float* sBG = sG + 192;   // beta_j e^{G_j} / |k_j|: column factor of T1
+  float* sDec = sG + 256;  // e^{G_L - G_j} / |k_j|: row factor of D'
+  float* sGp = sG + 320;   // G_j - log2(1/|k_j|): column exponent of A and P
+  float* sRk = sG + 384;   // 1/|k_j|
+  float* sRq = sG + 448;   // 1/|q_t|
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const GdnUnit u = p.units[blockIdx.x];
@@ -329,17 +374,20 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
         if (lane >= off) { a0 += y0; a1 += y1; }
       }
       a1 += __shfl_sync(0xffffffffu, a0, 31);
+      const float gl = __shfl_sync(0xffffffffu, a1, 31);  // padded tokens add nothing
+      const float b0 = gnext[2], b1 = gnext[3];
+      const float e0 = ex2(a0), e1 = ex2(a1);
       sG[lane] = a0;
       sG[lane + 32] = a1;
-      sB[lane] = gnext[2];
-      sB[lane + 32] = gnext[3];
-      if (c + 1 < nchunks) {
-        load_gates(ag, bg, p.hv_heads, t0 + kC, sd.len, lane, gnext);
-        float s = gnext[0] + gnext[1];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (lane == 0) sm.next_decay = __expf(s);
-      }
+      sB[lane] = b0;
+      sB[lane + 32] = b1;
+      sGq[lane] = scale * e0;
+      sGq[lane + 32] = scale * e1;
+      sBG[lane] = b0 * e0;
+      sBG[lane + 32] = b1 * e1;
+      sDec[lane] = ex2(gl - a0);
+      sDec[lane + 32] = ex2(gl - a1);
+      if (c + 1 < nchunks) load_gates(ag, bg, p.hv_heads, t0 + kC, sd.len, lane, gnext);
     }
 
     // ---- (2) wait for q, k, v; convert in place to fp16 (q, k normalised); zero past L ----
@@ -347,38 +395,53 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
     kq_inflight = false;
     if (!(ok = wait_all(&sm.bar_v, ph_v))) break;
     v_inflight = false;
+    if (tid == 0 && c + 1 < nchunks) {  // warm L2 with the next chunk's q, k, v
+      const int nrow = sd.tok_start + t0 + kC;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        tma_prefetch_l2_2d(&P.tk, hk * kD + 64 * r, nrow);
+        tma_prefetch_l2_2d(&P.tq, hk * kD + 64 * r, nrow);
+        tma_prefetch_l2_2d(&P.tv, h * kD + 64 * r, nrow);
+      }
+    }
     {
+      // raw bf16 -> fp16 in place (exact); rows past the chunk are zeroed. The norms are
+      // not applied to the tiles: they are folded into per-token factors below.
       const int j = tid & 15, rsub = tid >> 4;  // 16 threads per row, chunk j of the row
       const uint32_t reg = j >> 3, cc = j & 7;
-#pragma unroll 2
+      const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+      uint4 w[8];
+#pragma unroll
       for (int pass = 0; pass < 8; ++pass) {   // K rows 0-63, Q rows 64-127
-        const uint32_t r = pass * 16 + rsub, t = r & 63;
-        uint4* ptr = reinterpret_cast<uint4*>(sKQ + reg * 16384 + (r >> 3) * 1024 +
-                                              (r & 7) * 128 + ((cc ^ (r & 7)) << 4));
-        float x[8];
-        unpack_bf16x8(*ptr, x);
-        float ss = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ss += x[e] * x[e];
-#pragma unroll
-        for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        const float rn = (int)t < L ? (p.l2norm ? rsqrtf(ss + kL2NormEps) : 1.f) : 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] *= rn;
-        *ptr = pack_half8(x);
-      }
-#pragma unroll 2
-      for (int pass = 0; pass < 4; ++pass) {   // V rows 0-63
         const uint32_t r = pass * 16 + rsub;
-        uint4* ptr = reinterpret_cast<uint4*>(sV + reg * 8192 + (r >> 3) * 1024 +
-                                              (r & 7) * 128 + ((cc ^ (r & 7)) << 4));
-        float x[8];
-        unpack_bf16x8(*ptr, x);
-        if ((int)r >= L) {
+        w[pass] = *reinterpret_cast<const uint4*>(sKQ + reg * 16384 + (r >> 3) * 1024 +
+                                                  (r & 7) * 128 + ((cc ^ (r & 7)) << 4));
+      }
+      float ss[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      for (int pass = 0; pass < 8; ++pass) {
+        float x[8];
+        unpack_bf16x8(w[pass], x);
+        float a = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a += x[e] * x[e];
+        ss[pass] = a;
+        w[pass] = pack_half8(x);  // exact: bf16 values are fp16 values
+      }
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1)
+#pragma unroll
+        for (int pass = 0; pass < 8; ++pass) ss[pass] += __shfl_xor_sync(0xffffffffu, ss[pass], off);
+#pragma unroll
+      for (int pass = 0; pass < 8; ++pass) {
+        const uint32_t r = pass * 16 + rsub, t = r & 63;
+        const bool live = (int)t < L;
+        if (j == 0) {
+          const float rn = live ? (p.l2norm ? rsqrtf(ss[pass] + kL2NormEps) : 1.f) : 0.f;
+          (pass < 4 ? sRk : sRq)[t] = rn;
         }
-        *ptr = pack_half8(x);
+        *reinterpret_cast<uint4*>(sKQ + reg * 16384 + (r >> 3) * 1024 + (r & 7) * 128 +
+                                  ((cc ^ (r & 7)) << 4)) = live ? w[pass] : zero;
       }
     }
     publish_operands();
@@ -396,9 +459,39 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       mma_commit(&sm.bar_mma);
     }
     __syncwarp();
+    if (warp == 1) {  // fold the norms into the per-token factors
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int i = lane + 32 * hh;
+        const float rk = sRk[i], rq = sRq[i];
+        sGp[i] = sG[i] - __log2f(rk);  // +inf for padded tokens: their column terms vanish
+        sBG[i] *= rk;
+        sDec[i] *= rk;
+        sGq[i] *= rq;
+      }
+    }
+    {  // V rows 0-63 while M1 runs (V is first read by M3)
+      const int j = tid & 15, rsub = tid >> 4;
+      const uint32_t reg = j >> 3, cc = j & 7;
+      const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+      uint4 w[4];
+#pragma unroll
+      for (int pass = 0; pass < 4; ++pass) {
+        const uint32_t r = pass * 16 + rsub;
+        w[pass] = *reinterpret_cast<const uint4*>(sV + reg * 8192 + (r >> 3) * 1024 +
+                                                  (r & 7) * 128 + ((cc ^ (r & 7)) << 4));
+      }
+#pragma unroll
+      for (int pass = 0; pass < 4; ++pass) {
+        const uint32_t r = pass * 16 + rsub;
+        *reinterpret_cast<uint4*>(sV + reg * 8192 + (r >> 3) * 1024 + (r & 7) * 128 +
+                                  ((cc ^ (r & 7)) << 4)) =
+            (int)r < L ? bf16x8_to_half8(w[pass]) : zero;
+      }
+    }
     if (!(ok = wait_all(&sm.bar_mma, ph_mma))) break;
 
-    // ---- (4) A (rows 0-63, fp32) and P (rows 64-127, fp16) from R0; Q~ = e^G Q over Q -----
+    // ---- (4) A (rows 0-63, fp32) and P (rows 64-127, fp16); Q~ = scale e^G Q / |q| over Q -
     {
       uint32_t r[32];
       tmem_ld32(t_lane + TM_R0 + 32 * half, r);
@@ -406,64 +499,82 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       const int j0 = 32 * half;
       if (row < 64) {
         const int i = row;
-        const float gi = sG[i], bi = sB[i];
+        const float gi = sG[i] + __log2f(sB[i] * sRk[i]);  // row factor in the exponent
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
+          const float4 gj = *reinterpret_cast<const float4*>(sGp + j0 + e);
+          const float g4[4] = {gj.x, gj.y, gj.z, gj.w};
           float4 v;
           float* vv = reinterpret_cast<float*>(&v);
 #pragma unroll
           for (int f = 0; f < 4; ++f) {
-            const int j = j0 + e + f;
-            vv[f] = j < i ? bi * exp2f(gi - sG[j]) * __uint_as_float(r[e + f]) : 0.f;
+            const float x = __uint_as_float(r[e + f]) * ex2(gi - g4[f]);
+            vv[f] = j0 + e + f < i ? x : 0.f;
           }
           *reinterpret_cast<float4*>(sA + i * kLd + j0 + e) = v;
         }
       } else {
         const int t = row - 64;
-        const float gt = sG[t];
+        const float gt = sG[t] + __log2f(scale * sRq[t]);  // row factor in the exponent
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
+          const float4 ga = *reinterpret_cast<const float4*>(sGp + j0 + e);
+          const float4 gb = *reinterpret_cast<const float4*>(sGp + j0 + e + 4);
+          const float g8[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
           float x[8];
 #pragma unroll
           for (int f = 0; f < 8; ++f) {
-            const int j = j0 + e + f;
-            x[f] = j <= t ? exp2f(gt - sG[j]) * __uint_as_float(r[e + f]) : 0.f;
+            const float y = __uint_as_float(r[e + f]) * ex2(gt - g8[f]);
+            x[f] = j0 + e + f <= t ? y : 0.f;
           }
           st_chunk(sP, t, j0 + e, 64, x);
         }
-      }
-      // Q~ rows: Q row t scaled by e^{G_t} (M1 has consumed Q)
-      const int j = tid & 15, rsub = tid >> 4;
-      const uint32_t reg = j >> 3, cc = j & 7;
-#pragma unroll
-      for (int pass = 0; pass < 4; ++pass) {
-        const uint32_t t = pass * 16 + rsub, rr = 64 + t;
-        uint4* ptr = reinterpret_cast<uint4*>(sKQ + reg * 16384 + (rr >> 3) * 1024 +
-                                              (rr & 7) * 128 + ((cc ^ (rr & 7)) << 4));
-        float x[8];
-        unpack_half8(*ptr, x);
-        const float gm = exp2f(sG[t]);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] *= gm;
-        *ptr = pack_half8(x);
       }
     }
     tc_fence_before();
     __syncthreads();
 
     // ---- (5) T = (I + A)^-1; T1 = T diag(beta e^G), T2 = T diag(beta) (fp16) -----------------
-    invert_unit_lower(sA, sT, sXs, tid);
+    if (warp < 2) {
+      invert_diag_blocks(sA, sT, tid);
+    } else {  // Q~ rows while the diagonal blocks are inverted (M1 has consumed Q)
+      for (int idx = tid - 64; idx < 1024; idx += kThreads - 64) {
+        const uint32_t t = idx >> 4, j = idx & 15, rr = 64 + t;
+        const uint32_t reg = j >> 3, cc = j & 7;
+        uint4* ptr = reinterpret_cast<uint4*>(sKQ + reg * 16384 + (rr >> 3) * 1024 +
+                                              (rr & 7) * 128 + ((cc ^ (rr & 7)) << 4));
+        uint4 w = *ptr;
+        const __half2 gm = __float2half2_rn(sGq[t]);
+        uint32_t* u = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __half2 y = __hmul2(*reinterpret_cast<const __half2*>(&u[e]), gm);
+          u[e] = *reinterpret_cast<const uint32_t*>(&y);
+        }
+        *ptr = w;
+      }
+    }
+    __syncthreads();
+    invert_merge(sA, sT, sXs, tid);
     {
       const int i = tid >> 2, jb = (tid & 3) * 16;
 #pragma unroll
       for (int h8 = 0; h8 < 16; h8 += 8) {
         float x1[8], x2[8];
 #pragma unroll
-        for (int f = 0; f < 8; ++f) {
-          const int j = jb + h8 + f;
-          const float tij = j <= i ? sT[i * kLd + j] : 0.f;
-          x2[f] = tij * sB[j];
-          x1[f] = x2[f] * exp2f(sG[j]);
+        for (int q4 = 0; q4 < 8; q4 += 4) {
+          const int j = jb + h8 + q4;
+          const float4 tv = *reinterpret_cast<const float4*>(sT + i * kLd + j);
+          const float4 bv = *reinterpret_cast<const float4*>(sB + j);
+          const float4 gv = *reinterpret_cast<const float4*>(sBG + j);
+          const float t4[4] = {tv.x, tv.y, tv.z, tv.w}, b4[4] = {bv.x, bv.y, bv.z, bv.w},
+                      g4[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+          for (int f = 0; f < 4; ++f) {
+            const float tij = j + f <= i ? t4[f] : 0.f;
+            x2[q4 + f] = tij * b4[f];
+            x1[q4 + f] = tij * g4[f];
+          }
         }
         st_chunk(sT1, i, jb + h8, 64, x1);
         st_chunk(sT2, i, jb + h8, 64, x2);
@@ -527,17 +638,26 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       uint32_t r[32];
       tmem_ld32(t_lane + TM_R0 + 32 * half, r);
       tmem_ld_wait();
-      const float gL = sG[L - 1];
 #pragma unroll
       for (int e = 0; e < 32; e += 8) {
+        const float4 da = *reinterpret_cast<const float4*>(sDec + 32 * half + e);
+        const float4 db = *reinterpret_cast<const float4*>(sDec + 32 * half + e + 4);
+        const float d8[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
         float x[8], y[8];
 #pragma unroll
         for (int f = 0; f < 8; ++f) {
           x[f] = __uint_as_float(r[e + f]);
-          y[f] = x[f] * exp2f(gL - sG[32 * half + e + f]);
+          y[f] = x[f] * d8[f];
         }
         st_chunk(sWD, row, 32 * half + e, 128, x);
         st_chunk(sDp, row, 32 * half + e, 128, y);
+      }
+      // total decay of the next chunk, for the state pre-scale after this chunk
+      if (warp == 0 && c + 1 < nchunks) {
+        float s = gnext[0] + gnext[1];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (lane == 0) sm.next_decay = __expf(s);
       }
     }
     publish_operands();
@@ -577,10 +697,18 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       uint32_t r[32];
       tmem_ld32(t_lane + TM_R0 + 32 * half, r);
       tmem_ld_wait();
-      __nv_bfloat16* so = reinterpret_cast<__nv_bfloat16*>(sO);
+      // lanes 2m and 2m+1 hold value rows dv, dv+1: swap so that each lane owns one
+      // (dv, dv+1) pair of a token and stores it as one bf16x2 word
+      const bool odd = lane & 1;
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
-        so[(32 * half + e) * kD + row] = __float2bfloat16_rn(scale * __uint_as_float(r[e]));
+      for (int e = 0; e < 32; e += 2) {
+        const float mine_lo = __uint_as_float(r[e]), mine_hi = __uint_as_float(r[e + 1]);
+        const float other = __shfl_xor_sync(0xffffffffu, odd ? mine_lo : mine_hi, 1);
+        const int t = 32 * half + e + (odd ? 1 : 0);
+        const __nv_bfloat162 pr = odd ? __floats2bfloat162_rn(other, mine_hi)
+                                      : __floats2bfloat162_rn(mine_lo, other);
+        *reinterpret_cast<__nv_bfloat162*>(sO + t * 256 + (row & ~1u) * 2) = pr;
+      }
 
       const int pos = t0 + L;
       const bool emit = c_next < sd.ckpt_end && p.ckpt_pos[c_next] == pos;

@@ -79,6 +79,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase completes or about
+// `hint_ns` nanoseconds pass, instead of spinning on the issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.b32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded sleeping wait: at most `limit` tries of about `hint_ns` each, then false.
+__device__ __forceinline__ bool mbar_wait_sleep_bounded(uint64_t* bar, uint32_t parity,
+                                                        uint32_t hint_ns, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i)
+    if (mbar_try_wait_sleep(bar, parity, hint_ns)) return true;
+  return false;
+}
+
 // Bounded wait: gives up after `limit` polls (each poll may itself suspend briefly) and
 // returns false, so a lost arrival can never hang the GPU.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
@@ -107,8 +129,23 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t
       : "memory");
 }
 
+// Pull one box of a tensor into L2 ahead of its load (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// 2^x with the hardware approximation (relative error about 2^-22), flushing subnormals.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // ---- warp-level tf32 MMA (m16n8k8), used for small fp32 block products -----------------
@@ -129,23 +166,11 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// Three tf32 products with hi/lo splits of both operands (the lo*lo term dropped): about
-// fp32 accuracy from the tf32 tensor path.
-__device__ __forceinline__ void mma_tf32x3(float (&d)[4], const float (&a)[4],
+// d += a * b with fp32 fragments rounded to tf32 (round to nearest, ties away).
+__device__ __forceinline__ void mma_tf32_f(float (&d)[4], const float (&a)[4],
                                            const float (&b)[2]) {
-  uint32_t ah[4], al[4], bh[2], bl[2];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    ah[i] = to_tf32(a[i]);
-    al[i] = to_tf32(a[i] - __uint_as_float(ah[i]));
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    bh[i] = to_tf32(b[i]);
-    bl[i] = to_tf32(b[i] - __uint_as_float(bh[i]));
-  }
-  mma_tf32(d, al, bh);
-  mma_tf32(d, ah, bl);
+  const uint32_t ah[4] = {to_tf32(a[0]), to_tf32(a[1]), to_tf32(a[2]), to_tf32(a[3])};
+  const uint32_t bh[2] = {to_tf32(b[0]), to_tf32(b[1])};
   mma_tf32(d, ah, bh);
 }
 
