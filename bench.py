@@ -305,6 +305,10 @@ def run_gpu(args):
 
     # end to end through the public API with host buffers
     e2e = None if args.no_e2e else run_e2e(args, torch, gdn, h, buf, pack, stream, world, dev)
+    secondary = None
+    if not args.no_secondary and world == 1:
+        del buf
+        secondary = run_secondary(torch, gdn, I, h, stream, flush, hbm_gbs)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -322,13 +326,62 @@ def run_gpu(args):
             "dtype": "bf16", "data": "synthetic",
             "config": dict(WORKLOAD, parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
                            prompts=pack.num_seqs, tokens=T),
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "secondary": secondary,
             "gpu_launches": args.steps, "clocks": clocks.summary(),
         }), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def _time_events(torch, fn, stream, flush, steps=10, warmup=3):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    tot = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        e.synchronize()
+        tot += s.elapsed_time(e)
+    return tot / steps
+
+
+def run_secondary(torch, gdn, I, h, stream, flush, hbm_gbs):
+    """Other workloads of the same path, timed the same way (not the headline metric):
+    the ragged prefix-cache pack, 4 x 8K prompts, and the one-token decode step of 32
+    sequences (HBM-bound: every state byte read and written once)."""
+    out = {}
+    for name, pack in (("ragged_prefix_8", I.ragged_prefix()), ("long_4x8192", I.long_prompts())):
+        buf = gdn.to_device(pack)
+        ms = _time_events(torch, lambda: gdn.prefill(h, buf, stream), stream, flush)
+        B = algorithmic_bytes(pack.total_tokens, 16, 32, 128, pack.num_seqs, pack.num_ckpts,
+                              init=pack.init is not None)
+        out[name] = {"tokens": pack.total_tokens, "us": ms * 1e3,
+                     "tokens_per_s": pack.total_tokens / (ms / 1e3),
+                     "achieved_gbs": B / (ms / 1e3) / 1e9, "frac_hbm": B / (ms / 1e3) / 1e9 / hbm_gbs}
+        del buf
+    # decode: 32 sequences, states resumed from a pool
+    ms_step = I.mixed_step()
+    B = ms_step.dec_q.shape[0]
+    cfg = gdn.make_config(16, 32, 128)
+    up = lambda x: torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)  # noqa: E731
+    q, k, v = up(ms_step.dec_q), up(ms_step.dec_k), up(ms_step.dec_v)
+    a = torch.from_numpy(ms_step.dec_a).cuda()
+    beta = torch.from_numpy(ms_step.dec_beta).cuda()
+    pool = torch.from_numpy(ms_step.dec_states).cuda()
+    slots = torch.arange(B, dtype=torch.int32, device="cuda")
+    o = torch.empty((B, 32, 128), dtype=torch.bfloat16, device="cuda")
+    ms = _time_events(torch, lambda: gdn.gdn_decode_step(h, cfg, B, q, k, v, a, beta, pool, B,
+                                                         slots, o, stream), stream, flush)
+    dbytes = B * 32 * 128 * 128 * 4 * 2 + B * (2 * 16 * 128 * 2 + 2 * 32 * 128 * 2 + 2 * 32 * 4)
+    out["decode_32seq"] = {"sequences": B, "us": ms * 1e3, "achieved_gbs": dbytes / (ms / 1e3) / 1e9,
+                           "frac_hbm": dbytes / (ms / 1e3) / 1e9 / hbm_gbs}
+    return out
 
 
 def run_e2e(args, torch, gdn, h, buf, pack, stream, world, dev):
@@ -378,6 +431,8 @@ def main():
                     help="prompts of the wave in the timed CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the ragged, 8K-prompt and decode timings")
     ap.add_argument("--prompts", type=int, default=32,
                     help="prompts in the wave (32 for the metric; fewer only for profiling)")
     args = ap.parse_args()
