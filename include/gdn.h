@@ -54,7 +54,8 @@ typedef enum gdn_status {
   GDN_ERR_WORKSPACE_TOO_SMALL = 3,
   GDN_ERR_CUDA = 4,               /* a CUDA runtime call or launch failed             */
   GDN_ERR_DEVICE_TIMEOUT = 5,     /* a bounded device-side wait gave up               */
-  GDN_ERR_POOL_EXHAUSTED = 6      /* pinned snapshot pool range out of bounds         */
+  GDN_ERR_POOL_EXHAUSTED = 6,     /* pinned snapshot pool range out of bounds         */
+  GDN_ERR_BUSY = 7                /* the handle's prefill stream already has a prefill */
 } gdn_status;
 
 typedef enum gdn_dtype {
@@ -179,6 +180,37 @@ gdn_status gdn_checkpoint_copy_query(gdn_handle* handle);
 
 /* Block the calling host thread until every checkpoint copy issued so far has completed. */
 gdn_status gdn_checkpoint_copy_wait(gdn_handle* handle);
+
+/* Prefill on the handle's own stream, so that a prefill pass overlaps decode steps that
+ * keep running on the caller's streams ("run at most one in-flight prefill on an owned
+ * CUDA stream", pegainfer PR #786, Changes). Arguments as gdn_prefill_packed; the owned
+ * stream first waits for the work already queued on `after_stream` (the inputs'
+ * producer), then runs the prefill and records a completion event. At most one prefill
+ * is in flight per handle: while the previous one runs, the call returns GDN_ERR_BUSY
+ * and enqueues nothing. Completion: gdn_prefill_async_query (poll), _wait (block the
+ * host) or _join (make another stream wait on the device). gdn_handle_destroy drains the
+ * owned stream first. */
+gdn_status gdn_prefill_packed_async(gdn_handle* handle, const gdn_config* cfg,
+                                    int32_t num_seqs, const int32_t* cu_seqlens_host,
+                                    const void* q, const void* k, const void* v,
+                                    const float* a, const float* beta,
+                                    const float* initial_state,
+                                    const int32_t* ckpt_cu_host, const int32_t* ckpt_pos_host,
+                                    void* o, float* ckpt_states, float* final_states,
+                                    void* workspace, size_t workspace_bytes,
+                                    void* after_stream);
+
+/* GDN_OK when no prefill is in flight on the handle's stream (the last one completed),
+ * GDN_ERR_DEVICE_TIMEOUT while it is still running ("poll completion events while
+ * decode is active", pegainfer PR #786). */
+gdn_status gdn_prefill_async_query(gdn_handle* handle);
+
+/* Block the host until the in-flight prefill (if any) has completed ("wait explicitly
+ * when the last decoder retires", pegainfer PR #786). */
+gdn_status gdn_prefill_async_wait(gdn_handle* handle);
+
+/* Make `stream` wait on the device for the in-flight prefill (if any); returns at once. */
+gdn_status gdn_prefill_async_join(gdn_handle* handle, void* stream);
 
 /* One-token decode update for `batch` decoding sequences, each with its own fp32 state in
  * a caller-owned pool, updated in place (vllm.cpp "vLLM, online serving", packed GDN

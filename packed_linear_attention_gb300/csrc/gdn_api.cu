@@ -48,6 +48,11 @@ struct gdn_handle {
   StagingSlot slots[kStagingSlots];
   int next_slot = 0;
   int32_t kernel_pref = 0;
+  // the owned prefill stream: at most one prefill in flight on it
+  cudaStream_t prefill_stream = nullptr;
+  cudaEvent_t prefill_ready = nullptr;  // caller stream -> prefill stream
+  cudaEvent_t prefill_done = nullptr;
+  bool prefill_inflight = false;
 };
 
 namespace {
@@ -219,6 +224,7 @@ const char* gdn_status_string(int32_t s) {
     case GDN_ERR_CUDA: return "CUDA error";
     case GDN_ERR_DEVICE_TIMEOUT: return "device wait timed out or not finished";
     case GDN_ERR_POOL_EXHAUSTED: return "range outside the pinned snapshot pool";
+    case GDN_ERR_BUSY: return "a prefill is already in flight on the handle's stream";
     default: return "unknown status";
   }
 }
@@ -236,8 +242,11 @@ gdn_status gdn_handle_create(int32_t device, size_t pinned_pool_bytes, gdn_handl
   if (!h) return GDN_ERR_CUDA;
   h->device = device;
   bool ok = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&h->prefill_stream, cudaStreamNonBlocking) == cudaSuccess &&
             cudaEventCreateWithFlags(&h->compute_ready, cudaEventDisableTiming) == cudaSuccess &&
-            cudaEventCreateWithFlags(&h->copy_done, cudaEventDisableTiming) == cudaSuccess;
+            cudaEventCreateWithFlags(&h->copy_done, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h->prefill_ready, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h->prefill_done, cudaEventDisableTiming) == cudaSuccess;
   for (int i = 0; ok && i < kStagingSlots; ++i)
     ok = cudaEventCreateWithFlags(&h->slots[i].done, cudaEventDisableTiming) == cudaSuccess;
   if (ok && pinned_pool_bytes > 0) {
@@ -259,6 +268,8 @@ gdn_status gdn_handle_destroy(gdn_handle* h) {
   int prev = 0;
   cudaGetDevice(&prev);
   cudaSetDevice(h->device);
+  if (h->prefill_stream && cudaStreamSynchronize(h->prefill_stream) != cudaSuccess)
+    st = GDN_ERR_CUDA;
   if (h->side && cudaStreamSynchronize(h->side) != cudaSuccess) st = GDN_ERR_CUDA;
   for (int i = 0; i < kStagingSlots; ++i) {
     StagingSlot& s = h->slots[i];
@@ -266,6 +277,9 @@ gdn_status gdn_handle_destroy(gdn_handle* h) {
     if (s.done) cudaEventDestroy(s.done);
     if (s.host) cudaFreeHost(s.host);
   }
+  if (h->prefill_ready) cudaEventDestroy(h->prefill_ready);
+  if (h->prefill_done) cudaEventDestroy(h->prefill_done);
+  if (h->prefill_stream) cudaStreamDestroy(h->prefill_stream);
   if (h->compute_ready) cudaEventDestroy(h->compute_ready);
   if (h->copy_done) cudaEventDestroy(h->copy_done);
   if (h->side) cudaStreamDestroy(h->side);
@@ -460,6 +474,62 @@ gdn_status gdn_checkpoint_copy_wait(gdn_handle* h) {
   if (!h) return GDN_ERR_INVALID_ARGUMENT;
   if (!h->copy_pending) return GDN_OK;
   return cuda_status(cudaEventSynchronize(h->copy_done));
+}
+
+gdn_status gdn_prefill_packed_async(gdn_handle* h, const gdn_config* cfg, int32_t num_seqs,
+                                    const int32_t* cu, const void* q, const void* k,
+                                    const void* v, const float* a, const float* beta,
+                                    const float* init, const int32_t* ckpt_cu,
+                                    const int32_t* ckpt_pos, void* o, float* ckpt_states,
+                                    float* final_states, void* workspace,
+                                    size_t workspace_bytes, void* after_stream) {
+  if (!h) return GDN_ERR_INVALID_ARGUMENT;
+  if (h->prefill_inflight) {
+    const cudaError_t q0 = cudaEventQuery(h->prefill_done);
+    if (q0 == cudaErrorNotReady) return GDN_ERR_BUSY;
+    if (q0 != cudaSuccess) return GDN_ERR_CUDA;
+    h->prefill_inflight = false;
+  }
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (prev != h->device && cudaSetDevice(h->device) != cudaSuccess) return GDN_ERR_CUDA;
+  // the owned stream starts once the work already queued on after_stream is done
+  cudaError_t e = cudaEventRecord(h->prefill_ready, static_cast<cudaStream_t>(after_stream));
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->prefill_stream, h->prefill_ready, 0);
+  if (prev != h->device) cudaSetDevice(prev);
+  if (e != cudaSuccess) return GDN_ERR_CUDA;
+  gdn_status s = gdn_prefill_packed(h, cfg, num_seqs, cu, q, k, v, a, beta, init, ckpt_cu,
+                                    ckpt_pos, o, ckpt_states, final_states, workspace,
+                                    workspace_bytes, h->prefill_stream);
+  if (s != GDN_OK) return s;
+  if (cudaEventRecord(h->prefill_done, h->prefill_stream) != cudaSuccess) return GDN_ERR_CUDA;
+  h->prefill_inflight = true;
+  return GDN_OK;
+}
+
+gdn_status gdn_prefill_async_query(gdn_handle* h) {
+  if (!h) return GDN_ERR_INVALID_ARGUMENT;
+  if (!h->prefill_inflight) return GDN_OK;
+  const cudaError_t e = cudaEventQuery(h->prefill_done);
+  if (e == cudaErrorNotReady) return GDN_ERR_DEVICE_TIMEOUT;
+  if (e != cudaSuccess) return GDN_ERR_CUDA;
+  h->prefill_inflight = false;
+  return GDN_OK;
+}
+
+gdn_status gdn_prefill_async_wait(gdn_handle* h) {
+  if (!h) return GDN_ERR_INVALID_ARGUMENT;
+  if (!h->prefill_inflight) return GDN_OK;
+  if (cudaEventSynchronize(h->prefill_done) != cudaSuccess) return GDN_ERR_CUDA;
+  h->prefill_inflight = false;
+  return GDN_OK;
+}
+
+gdn_status gdn_prefill_async_join(gdn_handle* h, void* stream) {
+  if (!h) return GDN_ERR_INVALID_ARGUMENT;
+  if (!h->prefill_inflight) return GDN_OK;
+  return cuda_status(
+      cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), h->prefill_done, 0));
 }
 
 gdn_status gdn_decode_step(gdn_handle* h, const gdn_config* cfg, int32_t batch, const void* q,

@@ -25,6 +25,7 @@ GDN_ERR_WORKSPACE_TOO_SMALL = 3
 GDN_ERR_CUDA = 4
 GDN_ERR_DEVICE_TIMEOUT = 5
 GDN_ERR_POOL_EXHAUSTED = 6
+GDN_ERR_BUSY = 7
 GDN_F32 = 0
 GDN_BF16 = 1
 KERNEL_AUTO = 0
@@ -37,7 +38,8 @@ EXPORTS = (
     "gdn_prefill_packed", "gdn_read_device_status", "gdn_checkpoint_copy",
     "gdn_checkpoint_copy_query", "gdn_checkpoint_copy_wait", "gdn_decode_step",
     "gdn_ckpt_position", "gdn_mixed_budget", "gdn_prefill_worklist_host",
-    "gdn_prefill_packed_noalloc",
+    "gdn_prefill_packed_noalloc", "gdn_prefill_packed_async", "gdn_prefill_async_query",
+    "gdn_prefill_async_wait", "gdn_prefill_async_join",
 )
 
 
@@ -86,6 +88,11 @@ def load(path: str = LIB_PATH):
                                                  P, P]),
             "gdn_prefill_worklist_host": (I32, [P, CFG, I32, IP, IP, IP, P, SZ,
                                                 ctypes.POINTER(SZ)]),
+            "gdn_prefill_packed_async": (I32, [P, CFG, I32, IP, P, P, P, P, P, P, IP, IP, P, P,
+                                               P, P, SZ, P]),
+            "gdn_prefill_async_query": (I32, [P]),
+            "gdn_prefill_async_wait": (I32, [P]),
+            "gdn_prefill_async_join": (I32, [P, P]),
             "gdn_checkpoint_copy": (I32, [P, P, SZ, SZ, P]),
             "gdn_checkpoint_copy_query": (I32, [P]),
             "gdn_checkpoint_copy_wait": (I32, [P]),
@@ -204,6 +211,47 @@ def gdn_prefill_packed_noalloc(cfg, cu_seqlens, q, k, v, a, beta, initial_state,
     if raise_on_error:
         _check(st, "gdn_prefill_packed_noalloc")
     return st
+
+
+def gdn_prefill_packed_async(handle, cfg, cu_seqlens, q, k, v, a, beta, initial_state, ckpt_cu,
+                             ckpt_pos, o, ckpt_states, final_states, workspace, workspace_bytes,
+                             after_stream=None, *, raise_on_error=True) -> int:
+    """Prefill on the handle's own stream after the work queued on `after_stream`."""
+    num_seqs = len(cu_seqlens) - 1
+    st = load().gdn_prefill_packed_async(
+        handle, ctypes.byref(cfg), num_seqs, _i32(cu_seqlens), _addr(q), _addr(k), _addr(v),
+        _addr(a), _addr(beta), _addr(initial_state), _i32(ckpt_cu), _i32(ckpt_pos),
+        _addr(o), _addr(ckpt_states), _addr(final_states), _addr(workspace),
+        int(workspace_bytes), _stream(after_stream))
+    if raise_on_error:
+        _check(st, "gdn_prefill_packed_async")
+    return st
+
+
+def gdn_prefill_async_query(handle) -> bool:
+    """True when no prefill is in flight on the handle's stream."""
+    st = load().gdn_prefill_async_query(handle)
+    if st == GDN_ERR_DEVICE_TIMEOUT:
+        return False
+    _check(st, "gdn_prefill_async_query")
+    return True
+
+
+def gdn_prefill_async_wait(handle) -> None:
+    _check(load().gdn_prefill_async_wait(handle), "gdn_prefill_async_wait")
+
+
+def gdn_prefill_async_join(handle, stream=None) -> None:
+    _check(load().gdn_prefill_async_join(handle, _stream(stream)), "gdn_prefill_async_join")
+
+
+def prefill_async(handle, buf: "DeviceBuffers", after_stream=None, *, raise_on_error=True) -> int:
+    """gdn_prefill_packed_async on a DeviceBuffers bundle."""
+    return gdn_prefill_packed_async(handle, buf.cfg, buf.cu, buf.q, buf.k, buf.v, buf.a,
+                                    buf.beta, buf.init, buf.ckpt_cu, buf.ckpt_pos, buf.o,
+                                    buf.ckpt if buf.ckpt.numel() else None, buf.final,
+                                    buf.workspace, buf.workspace_bytes, after_stream,
+                                    raise_on_error=raise_on_error)
 
 
 def gdn_prefill_worklist_host(handle, cfg, cu_seqlens, ckpt_cu=None, ckpt_pos=None) -> dict:
