@@ -63,8 +63,18 @@ typedef enum gdn_dtype {
   GDN_BF16 = 1   /* q, k, v, o in bf16; a, beta and all states stay fp32 */
 } gdn_dtype;
 
-/* Layer shape. Supported: head_dim_k == head_dim_v in {64, 128}, num_v_heads a positive
- * multiple of num_k_heads, chunk_size == 64. */
+/* How the `a` and `beta` arrays of a call are read. */
+typedef enum gdn_gate_mode {
+  GDN_GATES_DIRECT = 0,  /* a = log-decay (g = exp(a)), beta = write strength, as given */
+  GDN_GATES_RAW = 1      /* raw projections of the Qwen3.5/3.6-style GDN layer, turned into
+                            gates in the kernel: a = -exp(A_log[h]) * softplus(a_raw +
+                            dt_bias[h]), beta = sigmoid(b_raw) (fp32 arithmetic) */
+} gdn_gate_mode;
+
+/* Layer shape and gate inputs. Supported: head_dim_k == head_dim_v in {64, 128},
+ * num_v_heads a positive multiple of num_k_heads, chunk_size == 64. With gate_mode ==
+ * GDN_GATES_RAW, a_log and dt_bias must be non-NULL device arrays of H_v floats (unused
+ * otherwise). */
 typedef struct gdn_config {
   int32_t num_k_heads;   /* H_k */
   int32_t num_v_heads;   /* H_v; value head h reads key head h / (H_v / H_k)       */
@@ -74,6 +84,9 @@ typedef struct gdn_config {
   float scale;           /* output scale, usually 1/sqrt(d_k)                       */
   int32_t qk_l2norm;     /* nonzero: q, k <- x / sqrt(x.x + 1e-6) per token and head */
   int32_t io_dtype;      /* gdn_dtype of q, k, v, o                                 */
+  int32_t gate_mode;     /* gdn_gate_mode of a and beta                              */
+  const float* a_log;    /* [H_v] device fp32 per-head log decay rate (GATES_RAW)    */
+  const float* dt_bias;  /* [H_v] device fp32 per-head bias of a_raw (GATES_RAW)     */
 } gdn_config;
 
 typedef struct gdn_handle gdn_handle;

@@ -69,6 +69,19 @@ def _f64(x):
     return None if x is None else np.ascontiguousarray(x, dtype=np.float64)
 
 
+def gates_from_raw(a_raw, b_raw, a_log, dt_bias):
+    """Gates of the Qwen3.5/3.6-style GDN layer from its raw projections, in fp64: per value
+    head h, log-decay a = -exp(A_log[h]) * softplus(a_raw + dt_bias[h]) (so g = exp(a))
+    and write strength beta = sigmoid(b_raw). a_raw, b_raw: [T, H_v]; a_log, dt_bias: [H_v]."""
+    a_raw = np.asarray(a_raw, dtype=np.float64)
+    b_raw = np.asarray(b_raw, dtype=np.float64)
+    x = a_raw + np.asarray(dt_bias, dtype=np.float64)[None, :]
+    softplus = np.logaddexp(0.0, x)
+    a = -np.exp(np.asarray(a_log, dtype=np.float64))[None, :] * softplus
+    beta = 1.0 / (1.0 + np.exp(-b_raw))
+    return a, beta
+
+
 def default_threads() -> int:
     return max(1, os.cpu_count() or 1)
 
@@ -107,9 +120,13 @@ def prefill_arrays(cu_seqlens, q, k, v, a, beta, init, ckpt_cu, ckpt_pos, *, sca
 
 
 def prefill(pack, threads=None):
-    """Oracle over a ``Pack`` from ``packed_linear_attention_gb300.inputs``."""
+    """Oracle over a ``Pack`` from ``packed_linear_attention_gb300.inputs`` (raw gate
+    inputs, when the pack has them, are turned into gates by gates_from_raw first)."""
+    a, beta = pack.a, pack.beta
+    if getattr(pack, "a_log", None) is not None:
+        a, beta = gates_from_raw(pack.a, pack.beta, pack.a_log, pack.dt_bias)
     return prefill_arrays(pack.cu_seqlens, pack.as_f32("q"), pack.as_f32("k"),
-                          pack.as_f32("v"), pack.a, pack.beta, pack.init, pack.ckpt_cu,
+                          pack.as_f32("v"), a, beta, pack.init, pack.ckpt_cu,
                           pack.ckpt_pos, scale=pack.scale, l2norm=pack.qk_l2norm,
                           threads=threads)
 

@@ -101,6 +101,10 @@ gdn_status check_config(const gdn_config* c) {
   if (c->num_v_heads % c->num_k_heads != 0) return GDN_ERR_INVALID_ARGUMENT;
   if (c->io_dtype != GDN_F32 && c->io_dtype != GDN_BF16) return GDN_ERR_INVALID_ARGUMENT;
   if (!std::isfinite(c->scale)) return GDN_ERR_INVALID_ARGUMENT;
+  if (c->gate_mode != GDN_GATES_DIRECT && c->gate_mode != GDN_GATES_RAW)
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (c->gate_mode == GDN_GATES_RAW && (!c->a_log || !c->dt_bias))
+    return GDN_ERR_INVALID_ARGUMENT;
   if (c->head_dim_k != c->head_dim_v) return GDN_ERR_UNSUPPORTED;
   if (c->head_dim_k != 64 && c->head_dim_k != 128) return GDN_ERR_UNSUPPORTED;
   if (c->chunk_size != 64) return GDN_ERR_UNSUPPORTED;
@@ -408,6 +412,9 @@ gdn_status gdn_prefill_packed(gdn_handle* h, const gdn_config* cfg, int32_t num_
     pa.scale = cfg->scale;
     pa.l2norm = cfg->qk_l2norm ? 1 : 0;
     pa.status = reinterpret_cast<int32_t*>(ws);
+    pa.gate_mode = cfg->gate_mode;
+    pa.a_log = cfg->a_log;
+    pa.dt_bias = cfg->dt_bias;
     int e = fam == kChunked ? gdn::launch_chunked_prefill(pa, T, stream)
                             : gdn::launch_recurrent_prefill(pa, D, cfg->io_dtype == GDN_BF16,
                                                             stream);
@@ -557,6 +564,9 @@ gdn_status gdn_decode_step(gdn_handle* h, const gdn_config* cfg, int32_t batch, 
   da.group = cfg->num_v_heads / cfg->num_k_heads;
   da.scale = cfg->scale;
   da.l2norm = cfg->qk_l2norm ? 1 : 0;
+  da.gate_mode = cfg->gate_mode;
+  da.a_log = cfg->a_log;
+  da.dt_bias = cfg->dt_bias;
   int prev = 0;
   if (cudaGetDevice(&prev) != cudaSuccess) return GDN_ERR_CUDA;
   if (prev != h->device && cudaSetDevice(h->device) != cudaSuccess) return GDN_ERR_CUDA;

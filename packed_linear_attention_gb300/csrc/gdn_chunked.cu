@@ -162,14 +162,24 @@ __device__ __forceinline__ void issue_v(const ChunkedParams& P, uint8_t* sV, uin
   tma_load_2d(sV + 8192, &P.tv, h * kD + 64, row, bar);
 }
 
-// Loads the log-decays and betas of the chunk starting at token t0 (warp 0 only).
+// Loads the log-decays and betas of the chunk starting at token t0 (warp 0 only); with raw
+// gate inputs they are turned into gates here. Tokens past the chunk get a = beta = 0.
 __device__ __forceinline__ void load_gates(const float* ag, const float* bg, size_t stride,
-                                           int t0, int len, int lane, float (&g)[4]) {
+                                           int t0, int len, int lane, bool raw,
+                                           float a_log, float dt_bias, float (&g)[4]) {
   const int L = min(kC, len - t0);
-  g[0] = lane < L ? __ldg(ag + (size_t)(t0 + lane) * stride) : 0.f;
-  g[1] = lane + 32 < L ? __ldg(ag + (size_t)(t0 + lane + 32) * stride) : 0.f;
-  g[2] = lane < L ? __ldg(bg + (size_t)(t0 + lane) * stride) : 0.f;
-  g[3] = lane + 32 < L ? __ldg(bg + (size_t)(t0 + lane + 32) * stride) : 0.f;
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int t = lane + 32 * hh;
+    float a = 0.f, b = 0.f;
+    if (t < L) {
+      a = __ldg(ag + (size_t)(t0 + t) * stride);
+      b = __ldg(bg + (size_t)(t0 + t) * stride);
+      if (raw) gate_from_raw(a_log, dt_bias, a, b);
+    }
+    g[hh] = a;
+    g[2 + hh] = b;
+  }
 }
 
 // One 16 x 8 output tile D = sum_k Ablk[r0.., k] * Bblk[k.., n0..] over k in [k_lo, k_hi)
@@ -317,8 +327,11 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
   }
   // gates of chunk 0 (warp 0 keeps the next chunk's gates in registers)
   float gnext[4] = {0.f, 0.f, 0.f, 0.f};
+  const bool raw = p.gate_mode == 1;
+  const float a_log = raw ? __ldg(p.a_log + h) : 0.f;
+  const float dt_bias = raw ? __ldg(p.dt_bias + h) : 0.f;
   if (warp == 0 && nchunks > 0) {
-    load_gates(ag, bg, p.hv_heads, 0, sd.len, lane, gnext);
+    load_gates(ag, bg, p.hv_heads, 0, sd.len, lane, raw, a_log, dt_bias, gnext);
     float s = gnext[0] + gnext[1];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
@@ -387,7 +400,8 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       sBG[lane + 32] = b1 * e1;
       sDec[lane] = ex2(gl - a0);
       sDec[lane + 32] = ex2(gl - a1);
-      if (c + 1 < nchunks) load_gates(ag, bg, p.hv_heads, t0 + kC, sd.len, lane, gnext);
+      if (c + 1 < nchunks)
+        load_gates(ag, bg, p.hv_heads, t0 + kC, sd.len, lane, raw, a_log, dt_bias, gnext);
     }
 
     // ---- (2) wait for q, k, v; convert in place to fp16 (q, k normalised); zero past L ----

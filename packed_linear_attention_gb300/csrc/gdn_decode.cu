@@ -80,8 +80,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs p) {
   float4 S[kVec];
 #pragma unroll
   for (int m = 0; m < kVec; ++m) S[m] = srow[sub + 4 * m];
-  const float g = __expf(p.a[(size_t)b * p.hv_heads + h]);
-  const float bb = p.beta[(size_t)b * p.hv_heads + h];
+  float ga = p.a[(size_t)b * p.hv_heads + h], bb = p.beta[(size_t)b * p.hv_heads + h];
+  if (p.gate_mode == 1) gate_from_raw(p.a_log[h], p.dt_bias[h], ga, bb);
+  const float g = __expf(ga);
   const float vi = ld_f32(static_cast<const T*>(p.v) + ((size_t)b * p.hv_heads + h) * D + row);
   __syncthreads();
 

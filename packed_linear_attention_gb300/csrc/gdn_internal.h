@@ -51,6 +51,9 @@ struct PrefillArgs {
   float scale;
   int32_t l2norm;
   int32_t* status;        // device status word (0 = ok) or nullptr
+  int32_t gate_mode;      // 0: a, beta as given; 1: raw projections (see gate_from_raw)
+  const float* a_log;     // [Hv] (gate_mode 1)
+  const float* dt_bias;   // [Hv] (gate_mode 1)
 };
 
 struct DecodeArgs {
@@ -68,9 +71,25 @@ struct DecodeArgs {
   int32_t group;
   float scale;
   int32_t l2norm;
+  int32_t gate_mode;
+  const float* a_log;
+  const float* dt_bias;
 };
 
 constexpr float kL2NormEps = 1e-6f;
+
+// Gates of the Qwen3.5/3.6-style GDN layer from its raw projections: per value head h,
+// a = -exp(A_log[h]) * softplus(a_raw + dt_bias[h]) (the log-decay, g = exp(a)) and
+// beta = sigmoid(b_raw). softplus switches to the identity above 20, where
+// log1p(exp(x)) equals x to fp32 precision.
+#ifdef __CUDACC__
+__device__ __forceinline__ void gate_from_raw(float a_log, float dt_bias, float& a, float& b) {
+  const float x = a + dt_bias;
+  const float sp = x > 20.f ? x : log1pf(expf(x));
+  a = -expf(a_log) * sp;
+  b = 1.f / (1.f + expf(-b));
+}
+#endif
 
 // Launchers (defined in the .cu files). Return a cudaError_t as int.
 int launch_recurrent_prefill(const PrefillArgs& a, int head_dim, bool bf16, void* stream);

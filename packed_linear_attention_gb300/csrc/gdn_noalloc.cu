@@ -118,6 +118,9 @@ extern "C" gdn_status gdn_prefill_packed_noalloc(const gdn_config* cfg, int32_t 
   pa.scale = cfg->scale;
   pa.l2norm = cfg->qk_l2norm ? 1 : 0;
   pa.status = reinterpret_cast<int32_t*>(scratch);
+  pa.gate_mode = cfg->gate_mode;
+  pa.a_log = cfg->a_log;
+  pa.dt_bias = cfg->dt_bias;
   const int e = plan.family == 2
                     ? gdn::launch_chunked_prefill(pa, T, stream)
                     : gdn::launch_recurrent_prefill(pa, D, cfg->io_dtype == GDN_BF16, stream);

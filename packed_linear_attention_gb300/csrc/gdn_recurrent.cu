@@ -107,8 +107,10 @@ recurrent_prefill_kernel(PrefillArgs p) {
       if (u.row0 + lane < u.row0 + u.nrows)
         sv[j][lane] = to_f32(v[(tok * p.hv_heads + h) * D + u.row0 + lane]);
       if (lane == 0) {
-        sg[j] = __expf(p.a[tok * p.hv_heads + h]);
-        sb[j] = p.beta[tok * p.hv_heads + h];
+        float a = p.a[tok * p.hv_heads + h], b = p.beta[tok * p.hv_heads + h];
+        if (p.gate_mode == 1) gate_from_raw(p.a_log[h], p.dt_bias[h], a, b);
+        sg[j] = __expf(a);
+        sb[j] = b;
       }
     }
     __syncthreads();

@@ -28,6 +28,8 @@ GDN_ERR_POOL_EXHAUSTED = 6
 GDN_ERR_BUSY = 7
 GDN_F32 = 0
 GDN_BF16 = 1
+GDN_GATES_DIRECT = 0
+GDN_GATES_RAW = 1
 KERNEL_AUTO = 0
 KERNEL_RECURRENT = 1
 
@@ -53,7 +55,9 @@ class gdn_config(ctypes.Structure):
     _fields_ = [("num_k_heads", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
                 ("head_dim_k", ctypes.c_int32), ("head_dim_v", ctypes.c_int32),
                 ("chunk_size", ctypes.c_int32), ("scale", ctypes.c_float),
-                ("qk_l2norm", ctypes.c_int32), ("io_dtype", ctypes.c_int32)]
+                ("qk_l2norm", ctypes.c_int32), ("io_dtype", ctypes.c_int32),
+                ("gate_mode", ctypes.c_int32), ("a_log", ctypes.c_void_p),
+                ("dt_bias", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -141,10 +145,14 @@ def _i32(a) -> ctypes.Array | None:
 
 
 def make_config(num_k_heads, num_v_heads, head_dim, *, scale=None, io_dtype=GDN_BF16,
-                chunk_size=64, qk_l2norm=True) -> gdn_config:
+                chunk_size=64, qk_l2norm=True, a_log=None, dt_bias=None) -> gdn_config:
+    """Layer config; passing a_log and dt_bias (device tensors of H_v floats) selects raw
+    gate inputs (GDN_GATES_RAW). The tensors must outlive every call using the config."""
+    raw = a_log is not None or dt_bias is not None
     return gdn_config(int(num_k_heads), int(num_v_heads), int(head_dim), int(head_dim),
                       int(chunk_size), float(scale if scale is not None else head_dim ** -0.5),
-                      1 if qk_l2norm else 0, int(io_dtype))
+                      1 if qk_l2norm else 0, int(io_dtype),
+                      GDN_GATES_RAW if raw else GDN_GATES_DIRECT, _addr(a_log), _addr(dt_bias))
 
 
 # ---- C entry points, same names -----------------------------------------------------------
@@ -349,6 +357,8 @@ class DeviceBuffers:
     final: object
     workspace: object
     workspace_bytes: int
+    a_log: object = None       # device tensors kept alive for the config's pointers
+    dt_bias: object = None
 
 
 def to_device(pack, device="cuda", cfg: gdn_config | None = None) -> DeviceBuffers:
@@ -356,10 +366,14 @@ def to_device(pack, device="cuda", cfg: gdn_config | None = None) -> DeviceBuffe
     import torch
 
     bf16 = pack.io_dtype == "bf16"
+    a_log = dt_bias = None
+    if getattr(pack, "a_log", None) is not None:
+        a_log = torch.from_numpy(np.ascontiguousarray(pack.a_log, np.float32)).to(device)
+        dt_bias = torch.from_numpy(np.ascontiguousarray(pack.dt_bias, np.float32)).to(device)
     if cfg is None:
         cfg = make_config(pack.num_k_heads, pack.num_v_heads, pack.head_dim, scale=pack.scale,
                           io_dtype=GDN_BF16 if bf16 else GDN_F32, chunk_size=pack.chunk_size,
-                          qk_l2norm=pack.qk_l2norm)
+                          qk_l2norm=pack.qk_l2norm, a_log=a_log, dt_bias=dt_bias)
 
     def up(x):
         if bf16 and x.dtype == np.uint16:
@@ -378,7 +392,7 @@ def to_device(pack, device="cuda", cfg: gdn_config | None = None) -> DeviceBuffe
         ckpt=torch.empty((max(C, 0), Hv, D, D), dtype=torch.float32, device=device),
         final=torch.empty((pack.num_seqs, Hv, D, D), dtype=torch.float32, device=device),
         workspace=torch.empty(ws_bytes, dtype=torch.uint8, device=device),
-        workspace_bytes=ws_bytes,
+        workspace_bytes=ws_bytes, a_log=a_log, dt_bias=dt_bias,
     )
 
 

@@ -75,6 +75,9 @@ class Pack:
     chunk_size: int = 64
     qk_l2norm: bool = True
     meta: dict = field(default_factory=dict)
+    # raw gate inputs: when set, a and beta hold the raw projections a_raw and b_raw
+    a_log: Optional[np.ndarray] = None     # [H_v] float32
+    dt_bias: Optional[np.ndarray] = None   # [H_v] float32
 
     @property
     def num_seqs(self) -> int:
@@ -279,6 +282,23 @@ def mixed_step(seed: int = 0, num_waiting: int = 8, num_decoding: int = 32,
                      dec_k=dk, dec_v=dv, dec_a=da, dec_beta=db, dec_states=ds)
 
 
+def with_raw_gates(p: Pack, seed: int = 0) -> Pack:
+    """The same pack with raw gate projections instead of gates, drawn like a freshly
+    initialised Qwen3.5/3.6-style GDN layer: a_raw, b_raw ~ N(0, 1); A = exp(A_log) ~ U(1, 16)
+    per value head; dt ~ log-uniform in [1e-3, 1e-1] with dt_bias = softplus^-1(dt)."""
+    rng = np.random.default_rng(seed + 7919)
+    T, Hv = p.a.shape
+    a_raw = _normal(rng, (T, Hv))
+    b_raw = _normal(rng, (T, Hv))
+    a_log = np.log(rng.uniform(1.0, 16.0, size=Hv)).astype(np.float32)
+    dt = np.exp(rng.uniform(np.log(1e-3), np.log(1e-1), size=Hv))
+    dt_bias = (dt + np.log(-np.expm1(-dt))).astype(np.float32)  # inverse softplus
+    q = Pack(**{f: getattr(p, f) for f in p.__dataclass_fields__})
+    q.a, q.beta, q.a_log, q.dt_bias = a_raw, b_raw, a_log, dt_bias
+    q.name = p.name + "_raw_gates"
+    return q
+
+
 def sub_pack(p: Pack, seqs, v_heads=None) -> Pack:
     """The same inputs restricted to some prompts and (optionally) some value heads with
     their key heads, for sampled comparisons at full size. Value heads are taken as whole
@@ -317,6 +337,8 @@ def sub_pack(p: Pack, seqs, v_heads=None) -> Pack:
         num_k_heads=len(k_heads), num_v_heads=len(v_order), head_dim=p.head_dim,
         io_dtype=p.io_dtype, scale=p.scale, chunk_size=p.chunk_size, qk_l2norm=p.qk_l2norm,
         meta=dict(parent=p.name, seqs=seqs, v_heads=v_order),
+        a_log=None if p.a_log is None else np.ascontiguousarray(p.a_log[v_order]),
+        dt_bias=None if p.dt_bias is None else np.ascontiguousarray(p.dt_bias[v_order]),
     )
 
 

@@ -149,3 +149,23 @@ def test_checkpoint_copy_bounds_without_pool(lib):
     # NULL handle is an argument error; no CUDA call is made
     assert lib.gdn_checkpoint_copy(None, ctypes.c_void_p(16), 16, 0, None) == \
         gdn.GDN_ERR_INVALID_ARGUMENT
+
+
+def test_gate_mode_validation(lib):
+    cu = [0, 100, 300]
+    ok = gdn.make_config(**CFG)
+    assert gdn.gdn_prefill_workspace_size(ok, cu) > 0
+    raw = gdn.make_config(**CFG)
+    raw.gate_mode = gdn.GDN_GATES_RAW                     # raw gates without A_log, dt_bias
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.gdn_prefill_workspace_size(raw, cu)
+    assert e.value.status == gdn.GDN_ERR_INVALID_ARGUMENT
+    raw.a_log, raw.dt_bias = 1 << 20, 2 << 20             # both given: accepted
+    assert gdn.gdn_prefill_workspace_size(raw, cu) > 0
+    raw.dt_bias = None
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_prefill_workspace_size(raw, cu)
+    bad = gdn.make_config(**CFG)
+    bad.gate_mode = 2
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_prefill_workspace_size(bad, cu)

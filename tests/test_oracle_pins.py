@@ -13,6 +13,7 @@ from fractions import Fraction as Fr
 
 import numpy as np
 import pytest
+import torch
 
 from oracle import ref
 from packed_linear_attention_gb300 import inputs as I
@@ -305,3 +306,50 @@ def test_oracle_rejects_bad_checkpoints():
                     ckpt_lists=[[11]])
     with pytest.raises(ValueError):
         ref.prefill(p)
+
+
+# ---- raw gate inputs: the GDN layer's gating from its projections -------------------------
+
+def test_raw_gates_special_values():
+    """a = -exp(A_log) softplus(a_raw + dt_bias), beta = sigmoid(b_raw) at points where the
+    functions have exact or limiting values."""
+    a_raw = np.array([[0.0, 0.0, 50.0, -50.0]])
+    b_raw = np.array([[0.0, 40.0, -40.0, 0.0]])
+    a_log = np.array([0.0, np.log(2.0), 0.0, 0.0])
+    dt_bias = np.array([0.0, 0.0, 0.0, 0.0])
+    a, beta = ref.gates_from_raw(a_raw, b_raw, a_log, dt_bias)
+    np.testing.assert_allclose(a[0, 0], -np.log(2.0), rtol=1e-15)        # softplus(0) = ln 2
+    np.testing.assert_allclose(a[0, 1], -2.0 * np.log(2.0), rtol=1e-15)  # exp(A_log) = 2
+    np.testing.assert_allclose(a[0, 2], -50.0, rtol=1e-15)               # softplus(x) ~ x
+    np.testing.assert_allclose(a[0, 3], -np.exp(-50.0), rtol=1e-12)      # ~ exp(x) far left
+    np.testing.assert_allclose(beta[0], [0.5, 1.0, np.exp(-40.0), 0.5], rtol=1e-12)
+    # dt_bias shifts the softplus argument
+    a2, _ = ref.gates_from_raw(np.array([[1.5]]), np.array([[0.0]]), np.array([0.0]),
+                               np.array([-1.5]))
+    np.testing.assert_allclose(a2[0, 0], -np.log(2.0), rtol=1e-15)
+
+
+def test_raw_gates_match_library_routines():
+    F = torch.nn.functional
+    rng = np.random.default_rng(16)
+    a_raw = rng.standard_normal((50, 6)) * 4
+    b_raw = rng.standard_normal((50, 6)) * 4
+    a_log = rng.uniform(-2, 3, 6)
+    dt_bias = rng.uniform(-5, 1, 6)
+    a, beta = ref.gates_from_raw(a_raw, b_raw, a_log, dt_bias)
+    x = torch.from_numpy(a_raw + dt_bias)
+    want_a = -torch.exp(torch.from_numpy(a_log)) * F.softplus(x, beta=1.0, threshold=1e9)
+    np.testing.assert_allclose(a, want_a.numpy(), rtol=1e-14)
+    np.testing.assert_allclose(beta, torch.sigmoid(torch.from_numpy(b_raw)).numpy(), rtol=1e-14)
+
+
+def test_raw_gate_pack_runs_the_same_recurrence():
+    p = I.make_pack([33, 70], num_k_heads=1, num_v_heads=2, head_dim=8, io_dtype="f32", seed=17)
+    r = I.with_raw_gates(p, seed=3)
+    o, _, f = ref.prefill(r)
+    a, beta = ref.gates_from_raw(r.a, r.beta, r.a_log, r.dt_bias)
+    o2, _, f2 = ref.prefill_arrays(r.cu_seqlens, r.as_f32("q"), r.as_f32("k"), r.as_f32("v"),
+                                   a, beta, None, None, None, scale=r.scale)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(f, f2)
+    assert np.all(a < 0) and np.all((beta > 0) & (beta < 1))
