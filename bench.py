@@ -65,14 +65,15 @@ def algorithmic_flops(T, Hk, Hv, d, C=64):
 MEASURED_TRAFFIC = {
     "sources": {
         "packed_linear_attention_gb300/csrc/gdn_chunked.cu":
-            "2b39b128886f8d13837c07f8aa349cc90822c7e2f1ce5d38523b896ce1d1dbdb",
+            "356fe705d8963b23f4194229c0dc532bcc6cb4589eeb0c31a9ffd3e093c46def",
         "packed_linear_attention_gb300/csrc/ptx_sm103.cuh":
-            "64d61b546bfb129891b84aa3cd5cb80bf4430ea3cd67490cbf1e14801b6b5dc9",
+            "8498eb56a00787588a767b984c67c5d12a16d2004d612b5cfb5d46edd45ac374",
+        "packed_linear_attention_gb300/csrc/gdn_tma.cu":
+            "6767277781b4efc4e5331a19f80a831271b6d2574cbfd7e56b833cd067998c0b",
     },
-    "read_bytes": 546.1e6,
-    "write_bytes": 359.2e6,
+    "read_bytes": 545.9e6,
+    "write_bytes": 359.3e6,
 }
-
 
 def measured_traffic():
     import hashlib
@@ -287,6 +288,11 @@ def run_gpu(args):
     ms_local = sum(per) / len(per)
     ms, value = aggregate(T, ms_local, world, dev)
 
+    # the chunked kernel's automatic schedule choice (same rule as the library's)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    schedule = ("chunked, throughput schedule" if N * Hv >= 6 * sms
+                else "chunked, pipelined schedule") + f" ({N * Hv} units on {sms} SMs)"
+
     # roofline of the prefill kernel (the only kernel of the step)
     hbm_gbs, tflops, peak_src = load_peaks()
     B = algorithmic_bytes(T, Hk, Hv, d, N, pack.num_ckpts)
@@ -325,7 +331,7 @@ def run_gpu(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
             "config": dict(WORKLOAD, parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
-                           prompts=pack.num_seqs, tokens=T),
+                           prompts=pack.num_seqs, tokens=T, schedule=schedule),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "secondary": secondary,
             "gpu_launches": args.steps, "clocks": clocks.summary(),
         }), flush=True)
@@ -362,6 +368,7 @@ def run_secondary(torch, gdn, I, h, stream, flush, hbm_gbs):
         B = algorithmic_bytes(pack.total_tokens, 16, 32, 128, pack.num_seqs, pack.num_ckpts,
                               init=pack.init is not None)
         out[name] = {"tokens": pack.total_tokens, "us": ms * 1e3,
+                     "schedule": "chunked, pipelined (automatic choice: few units per SM)",
                      "tokens_per_s": pack.total_tokens / (ms / 1e3),
                      "achieved_gbs": B / (ms / 1e3) / 1e9, "frac_hbm": B / (ms / 1e3) / 1e9 / hbm_gbs}
         del buf

@@ -112,10 +112,17 @@ gdn_status gdn_handle_destroy(gdn_handle* handle);
 /* Host address and size of the handle's pinned snapshot pool. */
 gdn_status gdn_pool_info(gdn_handle* handle, void** host_ptr, size_t* bytes);
 
-/* Kernel choice for later prefill calls on this handle: 0 = automatic (the tensor-core
- * chunked kernel where it applies: bf16 io, d = 128; otherwise the token-serial CUDA-core
- * kernel), 1 = always the token-serial kernel (a cross-check path). Errors:
- * INVALID_ARGUMENT. */
+/* Kernel choice for later prefill calls on this handle:
+ *   0 = automatic: the tensor-core chunked kernel where it applies (bf16 io, d = 128),
+ *       in its throughput schedule (two CTAs per SM) when the pack has at least six
+ *       (prompt, value head) units per SM, else in its pipelined schedule (one CTA per SM,
+ *       the next chunk's state-independent work overlapped with the current recurrence);
+ *       otherwise the token-serial CUDA-core kernel;
+ *   1 = always the token-serial kernel (a cross-check path);
+ *   2 = the chunked kernel's pipelined schedule, 3 = its throughput schedule (where the
+ *       chunked kernel applies; otherwise the token-serial kernel).
+ * Every choice computes the same recurrence; results agree to rounding (each schedule is
+ * deterministic and packing-independent on its own). Errors: INVALID_ARGUMENT. */
 gdn_status gdn_set_kernel_preference(gdn_handle* handle, int32_t preference);
 
 /* Device workspace bytes that gdn_prefill_packed needs for this pack (the chunk/tile work

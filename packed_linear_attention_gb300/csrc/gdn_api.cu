@@ -301,7 +301,7 @@ gdn_status gdn_pool_info(gdn_handle* h, void** host_ptr, size_t* bytes) {
 }
 
 gdn_status gdn_set_kernel_preference(gdn_handle* h, int32_t pref) {
-  if (!h || pref < 0 || pref > 1) return GDN_ERR_INVALID_ARGUMENT;
+  if (!h || pref < 0 || pref > 3) return GDN_ERR_INVALID_ARGUMENT;
   h->kernel_pref = pref;
   return GDN_OK;
 }
@@ -415,7 +415,8 @@ gdn_status gdn_prefill_packed(gdn_handle* h, const gdn_config* cfg, int32_t num_
     pa.gate_mode = cfg->gate_mode;
     pa.a_log = cfg->a_log;
     pa.dt_bias = cfg->dt_bias;
-    int e = fam == kChunked ? gdn::launch_chunked_prefill(pa, T, stream)
+    const int schedule = h->kernel_pref >= 2 ? h->kernel_pref : gdn::kChunkedAuto;
+    int e = fam == kChunked ? gdn::launch_chunked_prefill(pa, T, schedule, stream)
                             : gdn::launch_recurrent_prefill(pa, D, cfg->io_dtype == GDN_BF16,
                                                             stream);
     if (e != 0) s = GDN_ERR_CUDA;

@@ -1,4 +1,5 @@
-// gdn_chunked.cu — chunked gated-delta-rule prefill on the tcgen05 tensor cores (sm_103a).
+// gdn_chunked.cu — chunked gated-delta-rule prefill on the tcgen05 tensor cores (sm_103a),
+// throughput schedule.
 //
 // Method (Gated Delta Networks, Yang, Kautz & Hatamizadeh, 2024, in its chunked UT/WY
 // form). Per (prompt, value head) unit the state S (d_v x d_k = 128 x 128, fp32) is carried
@@ -16,10 +17,13 @@
 // accumulation; q and k are normalised in fp32 before their rounding, v is widened exactly
 // from bf16, and the fp32 state lives in TMEM for the whole prompt (its fp16 copy feeds
 // the MMAs and is refreshed every chunk). The 64x64 triangular inverse is fp32 (diagonal
-// blocks by forward substitution, off-diagonal blocks by warp-level 3xTF32 products).
+// blocks by forward substitution, off-diagonal blocks by warp-level tf32 products).
 // Operands must stay inside the fp16 range (|v| and state entries below 65504).
 //
-// Per CTA (256 threads, 8 warps, two CTAs per SM): one unit, chunks in order.
+// Throughput schedule: per CTA (256 threads, 8 warps, two CTAs per SM) one unit, the
+// phases of each chunk in sequence; the two CTAs of an SM hide each other's latencies.
+// The pipelined schedule (gdn_chunked_pipe.cu) computes the same chunk algebra with one
+// 16-warp CTA per SM; launch_chunked_prefill picks between them.
 //   TMEM (256 columns): [0,64) R0 = the current product (fp32); [64,128) S16 = fp16 state
 //   copy (A operand of the state products); [128,256) S32 = fp32 state, accumulated in
 //   place by the update product.
@@ -33,7 +37,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "gdn_internal.h"
 #include "ptx_sm103.cuh"
@@ -805,70 +808,23 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
   if (warp == 0) tmem_dealloc(tbase, TM_COLS);
 }
 
-// ---- host: tensor maps ------------------------------------------------------------------
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  return fn;
-}
-
-// 2D map over a [rows][cols] bf16 matrix (row stride = cols), 64 x 64 boxes, 128B swizzle;
-// reads past the last row return zeros.
-bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {64, 64};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
-}
-
 }  // namespace
 
-int chunked_prefill_smem_bytes() { return (int)SMEM_BYTES; }
-
-int launch_chunked_prefill(const PrefillArgs& a, int64_t total_tokens, void* stream) {
+int launch_chunked_throughput(const PrefillArgs& a, int64_t total_tokens, void* stream) {
   if (a.num_units == 0) return 0;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(chunked_prefill_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(
+        chunked_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return (int)e;
     configured = true;
   }
   ChunkedParams P;
   P.a = a;
-  const uint64_t rows = total_tokens > 0 ? (uint64_t)total_tokens : 1;
-  if (total_tokens > 0) {
-    if (!make_map(&P.tq, a.q, (uint64_t)a.hk_heads * kD, rows) ||
-        !make_map(&P.tk, a.k, (uint64_t)a.hk_heads * kD, rows) ||
-        !make_map(&P.tv, a.v, (uint64_t)a.hv_heads * kD, rows))
-      return (int)cudaErrorInvalidValue;
-  } else {
-    memset(&P.tq, 0, sizeof(CUtensorMap));
-    memset(&P.tk, 0, sizeof(CUtensorMap));
-    memset(&P.tv, 0, sizeof(CUtensorMap));
-  }
-  chunked_prefill_kernel<<<a.num_units, kThreads, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(P);
+  if (!make_qkv_maps(a, total_tokens, kD, &P.tq, &P.tk, &P.tv))
+    return (int)cudaErrorInvalidValue;
+  chunked_prefill_kernel<<<a.num_units, kThreads, SMEM_BYTES,
+                                 static_cast<cudaStream_t>(stream)>>>(P);
   return (int)cudaGetLastError();
 }
 

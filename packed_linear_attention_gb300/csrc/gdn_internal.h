@@ -9,6 +9,8 @@
 // block. Units are ordered longest prompt first so the hardware block scheduler, which
 // hands out blocks roughly in index order, runs a longest-processing-time-first schedule.
 #pragma once
+#include <cuda.h>
+
 #include <cstddef>
 #include <cstdint>
 
@@ -94,8 +96,27 @@ __device__ __forceinline__ void gate_from_raw(float a_log, float dt_bias, float&
 // Launchers (defined in the .cu files). Return a cudaError_t as int.
 int launch_recurrent_prefill(const PrefillArgs& a, int head_dim, bool bf16, void* stream);
 int launch_decode(const DecodeArgs& a, int head_dim, bool bf16, void* stream);
-int launch_chunked_prefill(const PrefillArgs& a, int64_t total_tokens, void* stream);
-int chunked_prefill_smem_bytes();
+
+// The chunked tensor-core prefill has two schedules over the same work list (one unit per
+// prompt and value head):
+//  * throughput (gdn_chunked.cu): two 8-warp CTAs per SM, each running its unit's chunk
+//    phases in sequence; best when every SM has several units to run;
+//  * pipelined (gdn_chunked_pipe.cu): one 16-warp CTA per SM whose two warp groups overlap
+//    the state-independent work of the next chunk with the recurrence of the current one;
+//    shortest time per unit, so best for packs with few units per SM or very long prompts.
+// kChunkedAuto takes the throughput schedule when the pack has at least
+// kThroughputUnitsPerSM units per SM.
+enum ChunkedSchedule : int { kChunkedAuto = 0, kChunkedPipelined = 2, kChunkedThroughput = 3 };
+constexpr int kThroughputUnitsPerSM = 6;
+int launch_chunked_throughput(const PrefillArgs& a, int64_t total_tokens, void* stream);
+int launch_chunked_pipelined(const PrefillArgs& a, int64_t total_tokens, void* stream);
+int launch_chunked_prefill(const PrefillArgs& a, int64_t total_tokens, int schedule,
+                           void* stream);
+
+// 2D bf16 tensor maps (64 x 64 boxes, 128-byte swizzle, zero fill past the last row) over
+// q, k (H_k * d columns) and v (H_v * d columns) with total_tokens rows (gdn_tma.cu).
+bool make_qkv_maps(const PrefillArgs& a, int64_t total_tokens, int head_dim, CUtensorMap* tq,
+                   CUtensorMap* tk, CUtensorMap* tv);
 
 // Host-side planning shared with the allocation-free entry point (gdn_noalloc.cu):
 // the kernel family, the work-list layout and its size for one pack.

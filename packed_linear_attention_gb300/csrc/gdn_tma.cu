@@ -1,0 +1,85 @@
+// gdn_tma.cu — 2D TMA tensor maps over the packed bf16 q, k, v matrices.
+//
+// The chunked prefill kernels load 64-token x 64-column boxes of q, k and v with
+// cp.async.bulk.tensor; this file encodes the maps through the driver's
+// cuTensorMapEncodeTiled, fetched once through the runtime's entry-point query.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+}  // namespace
+
+bool make_bf16_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+bool make_qkv_maps(const PrefillArgs& a, int64_t total_tokens, int head_dim, CUtensorMap* tq,
+                   CUtensorMap* tk, CUtensorMap* tv) {
+  if (total_tokens <= 0) {
+    memset(tq, 0, sizeof(CUtensorMap));
+    memset(tk, 0, sizeof(CUtensorMap));
+    memset(tv, 0, sizeof(CUtensorMap));
+    return true;
+  }
+  const uint64_t rows = (uint64_t)total_tokens;
+  return make_bf16_map(tq, a.q, (uint64_t)a.hk_heads * head_dim, rows) &&
+         make_bf16_map(tk, a.k, (uint64_t)a.hk_heads * head_dim, rows) &&
+         make_bf16_map(tv, a.v, (uint64_t)a.hv_heads * head_dim, rows);
+}
+
+int launch_chunked_prefill(const PrefillArgs& a, int64_t total_tokens, int schedule,
+                           void* stream) {
+  if (schedule == kChunkedAuto) {
+    static int sms[64] = {0};  // SM count per device, asked once
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return (int)e;
+    int n = dev >= 0 && dev < 64 ? sms[dev] : 0;
+    if (n == 0) {
+      e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return (int)e;
+      if (dev >= 0 && dev < 64) sms[dev] = n;
+    }
+    schedule = (int64_t)a.num_units >= (int64_t)kThroughputUnitsPerSM * n ? kChunkedThroughput
+                                                                          : kChunkedPipelined;
+  }
+  return schedule == kChunkedThroughput ? launch_chunked_throughput(a, total_tokens, stream)
+                                        : launch_chunked_pipelined(a, total_tokens, stream);
+}
+
+}  // namespace gdn

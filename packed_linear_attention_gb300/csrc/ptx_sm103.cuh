@@ -116,6 +116,31 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// Plain arrival (count 1) on an mbarrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// ---- named barriers (a subset of the block's warps) ---------------------------------------
+
+// Barrier `id` (1-15; 0 is the block-wide __syncthreads barrier) over `nthreads` threads,
+// a multiple of 32; every warp taking part executes it.
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// The same barrier with an OR-reduction of `pred` over the participating threads.
+__device__ __forceinline__ bool named_any(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // ---- TMA (tensor copies global -> shared, completion counted on an mbarrier) ------------
 
 // 2D tiled load of one box at coordinates (x = innermost, y); x * element size must be a

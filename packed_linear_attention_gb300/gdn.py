@@ -32,6 +32,8 @@ GDN_GATES_DIRECT = 0
 GDN_GATES_RAW = 1
 KERNEL_AUTO = 0
 KERNEL_RECURRENT = 1
+KERNEL_CHUNKED_PIPELINED = 2
+KERNEL_CHUNKED_THROUGHPUT = 3
 
 # every symbol include/gdn.h declares
 EXPORTS = (

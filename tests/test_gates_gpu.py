@@ -28,7 +28,8 @@ def test_raw_gates_tiny_f32(pref):
     assert_close(fin, rfin, "f32", "final")
 
 
-@pytest.mark.parametrize("pref", KERNELS)
+@pytest.mark.parametrize("pref", KERNELS + [gdn.KERNEL_CHUNKED_PIPELINED,
+                                            gdn.KERNEL_CHUNKED_THROUGHPUT])
 def test_raw_gates_edge_lengths_bf16_d128(pref):
     torch_cuda()
     lengths = [1, 0, 63, 64, 65, 129, 200, 3]

@@ -17,6 +17,8 @@ from gpu_util import assert_close, compare_units, run, torch_cuda
 pytestmark = pytest.mark.gpu
 
 KERNELS = [gdn.KERNEL_AUTO, gdn.KERNEL_RECURRENT]
+# the two schedules of the chunked tensor-core kernel (bf16 io, d = 128 packs)
+CHUNKED = [gdn.KERNEL_CHUNKED_PIPELINED, gdn.KERNEL_CHUNKED_THROUGHPUT]
 
 
 @pytest.fixture(scope="module")
@@ -52,7 +54,7 @@ def test_tiny_dims_bf16(pref):
     compare_units(p, got, list(range(4)), list(range(4)))
 
 
-@pytest.mark.parametrize("pref", KERNELS)
+@pytest.mark.parametrize("pref", KERNELS + CHUNKED)
 def test_edge_lengths_d128(pref):
     """Empty prompts, single tokens, chunk-1/chunk/chunk+1 tails, checkpoints at ends."""
     torch_cuda()
@@ -67,11 +69,13 @@ def test_edge_lengths_d128(pref):
         np.testing.assert_array_equal(got[2][n], p.init[n].astype(np.float64))
 
 
-def test_chat_wave_full_size_sampled(wave):
-    """The 32 x 1,024 wave at full size, in the bench's launch configuration; sampled
-    prompts and value heads (both members of two GQA groups) against the oracle."""
+@pytest.mark.parametrize("pref", [gdn.KERNEL_AUTO, gdn.KERNEL_CHUNKED_PIPELINED])
+def test_chat_wave_full_size_sampled(wave, pref):
+    """The 32 x 1,024 wave at full size, in the bench's launch configuration (automatic
+    choice: the throughput schedule) and in the pipelined schedule; sampled prompts and value
+    heads (both members of two GQA groups) against the oracle."""
     torch_cuda()
-    got = run(wave)
+    got = run(wave, pref)
     compare_units(wave, got, [0, 13, 31], [0, 1, 30, 31])
 
 
@@ -79,17 +83,19 @@ def test_chat_wave_checkpoint_is_at_768(wave):
     assert wave.ckpt_pos.tolist() == [768] * 32
 
 
-def test_ragged_prefix_full(ragged):
+@pytest.mark.parametrize("pref", CHUNKED)
+def test_ragged_prefix_full(ragged, pref):
     torch_cuda()
-    got = run(ragged)
+    got = run(ragged, pref)
     compare_units(ragged, got, list(range(ragged.num_seqs)), [0, 1, 14, 15, 30, 31])
 
 
-def test_ragged_resume_from_checkpoint_equals_uninterrupted(ragged):
+@pytest.mark.parametrize("pref", CHUNKED)
+def test_ragged_resume_from_checkpoint_equals_uninterrupted(ragged, pref):
     """Prefill to a checkpoint, resume from it: equal to the uninterrupted run (bitwise
     when the cut is on the chunk grid, as every checkpoint here is)."""
     torch = torch_cuda()
-    full = run(ragged)
+    full = run(ragged, pref)
     # pick prompt 0 and its second checkpoint
     n = 0
     j0 = int(ragged.ckpt_cu[n])
@@ -102,19 +108,20 @@ def test_ragged_resume_from_checkpoint_equals_uninterrupted(ragged):
                   ckpt_cu=np.zeros(2, np.int32), ckpt_pos=np.zeros(0, np.int32),
                   num_k_heads=ragged.num_k_heads, num_v_heads=ragged.num_v_heads,
                   head_dim=ragged.head_dim, io_dtype="bf16", scale=ragged.scale)
-    o2, _, fin2 = run(rest)
+    o2, _, fin2 = run(rest, pref)
     np.testing.assert_array_equal(o2, full[0][s + cut:e])
     np.testing.assert_array_equal(fin2[0], full[2][n])
 
 
-def test_long_prompts_sampled():
+@pytest.mark.parametrize("pref", CHUNKED)
+def test_long_prompts_sampled(pref):
     torch_cuda()
     p = I.long_prompts()
-    got = run(p)
+    got = run(p, pref)
     compare_units(p, got, [1, 3], [2, 3, 20, 21])
 
 
-@pytest.mark.parametrize("pref", KERNELS)
+@pytest.mark.parametrize("pref", KERNELS + CHUNKED)
 def test_pack_vs_alone_bitwise(pref):
     """Each prompt alone and inside the pack: identical o, checkpoints and final state."""
     torch_cuda()
@@ -131,7 +138,7 @@ def test_pack_vs_alone_bitwise(pref):
         np.testing.assert_array_equal(f[n], f1[0])
 
 
-@pytest.mark.parametrize("pref", KERNELS)
+@pytest.mark.parametrize("pref", KERNELS + CHUNKED)
 def test_determinism(pref):
     torch_cuda()
     p = I.make_pack([500, 77, 1024], num_k_heads=4, num_v_heads=8, head_dim=128,
@@ -142,23 +149,22 @@ def test_determinism(pref):
         np.testing.assert_array_equal(x, y)
 
 
-def test_in_place_final_over_initial():
+@pytest.mark.parametrize("pref", CHUNKED)
+def test_in_place_final_over_initial(pref):
     torch = torch_cuda()
     p = I.make_pack([130, 64], num_k_heads=2, num_v_heads=4, head_dim=128, io_dtype="bf16",
                     seed=6, init_std=0.02)
-    want = run(p)
+    want = run(p, pref)
     buf = gdn.to_device(p)
     buf.final = buf.init  # final_states aliases initial_state
-    from gpu_util import handle
-    gdn.prefill(handle(), buf)
-    torch.cuda.synchronize()
+    run(p, pref, buf=buf)
     np.testing.assert_array_equal(buf.init.cpu().numpy().astype(np.float64), want[2])
 
 
-def test_guard_bands_untouched():
+@pytest.mark.parametrize("pref", CHUNKED)
+def test_guard_bands_untouched(pref):
     """Outputs are written exactly inside their buffers: canaries around each survive."""
     torch = torch_cuda()
-    from gpu_util import handle
     lengths = [65, 1, 130]
     p = I.make_pack(lengths, num_k_heads=2, num_v_heads=4, head_dim=128, io_dtype="bf16",
                     seed=7, init_std=0.02, ckpt_lists=[[64, 65], [1], [128]])
@@ -172,8 +178,7 @@ def test_guard_bands_untouched():
     o_big, buf.o = guarded(buf.o)
     c_big, buf.ckpt = guarded(buf.ckpt)
     f_big, buf.final = guarded(buf.final)
-    gdn.prefill(handle(), buf)
-    torch.cuda.synchronize()
+    run(p, pref, buf=buf)
     for big in (o_big, c_big, f_big):
         assert torch.isnan(big[:G].float()).all() and torch.isnan(big[-G:].float()).all()
         assert not torch.isnan(big[G:-G].float()).any()
@@ -199,3 +204,18 @@ def test_checkpoint_copy_to_pinned_pool(ragged):
     np.testing.assert_array_equal(host.reshape(buf.ckpt.shape), buf.ckpt.cpu().numpy())
     with pytest.raises(gdn.GdnError):
         gdn.gdn_checkpoint_copy(h, buf.ckpt, size, 16, stream)
+
+
+def test_automatic_schedule_choice(wave):
+    """Automatic choice: the pipelined schedule for a pack with few units per SM, the
+    throughput schedule for the full wave (the schedules round differently, so a bitwise
+    match identifies the one that ran)."""
+    torch_cuda()
+    small = I.make_pack([200, 64, 900], num_k_heads=16, num_v_heads=32, head_dim=128,
+                        io_dtype="bf16", seed=8, init_std=0.02)
+    auto = run(small)
+    for x, y in zip(auto, run(small, gdn.KERNEL_CHUNKED_PIPELINED)):
+        np.testing.assert_array_equal(x, y)
+    auto = run(wave)
+    for x, y in zip(auto, run(wave, gdn.KERNEL_CHUNKED_THROUGHPUT)):
+        np.testing.assert_array_equal(x, y)
