@@ -313,8 +313,10 @@ def run_gpu(args):
     e2e = None if args.no_e2e else run_e2e(args, torch, gdn, h, buf, pack, stream, world, dev)
     secondary = None
     if not args.no_secondary and world == 1:
+        until_d2h = run_until_ckpt_d2h(torch, gdn, h, buf, stream, flush)
         del buf
         secondary = run_secondary(torch, gdn, I, h, stream, flush, hbm_gbs)
+        secondary["wave_until_ckpt_d2h"] = until_d2h
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -357,6 +359,28 @@ def _time_events(torch, fn, stream, flush, steps=10, warmup=3):
     return tot / steps
 
 
+def run_until_ckpt_d2h(torch, gdn, h, buf, stream, flush, steps=10):
+    """The wave's prefill followed by the copy of its checkpoints into the handle's pinned
+    pool (side stream), timed on the host from the launch until the copy has completed
+    (inputs resident, L2 flushed first)."""
+    nbytes = buf.ckpt.numel() * 4
+    for _ in range(3):
+        gdn.prefill(h, buf, stream)
+        gdn.gdn_checkpoint_copy(h, buf.ckpt, nbytes, 0, stream)
+        gdn.gdn_checkpoint_copy_wait(h)
+    tot = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        gdn.prefill(h, buf, stream)
+        gdn.gdn_checkpoint_copy(h, buf.ckpt, nbytes, 0, stream)
+        gdn.gdn_checkpoint_copy_wait(h)
+        tot += time.perf_counter() - t0
+    us = tot / steps * 1e6
+    return {"us": us, "ckpt_bytes": nbytes, "timing": "host clock, launch to copy completion"}
+
+
 def run_secondary(torch, gdn, I, h, stream, flush, hbm_gbs):
     """Other workloads of the same path, timed the same way (not the headline metric):
     the ragged prefix-cache pack, 4 x 8K prompts, and the one-token decode step of 32
@@ -372,6 +396,29 @@ def run_secondary(torch, gdn, I, h, stream, flush, hbm_gbs):
                      "tokens_per_s": pack.total_tokens / (ms / 1e3),
                      "achieved_gbs": B / (ms / 1e3) / 1e9, "frac_hbm": B / (ms / 1e3) / 1e9 / hbm_gbs}
         del buf
+    # one 32K-token prompt: whole (32 units) and split into 3 and 4 parallel segments
+    pack = I.single_long_prompt()
+    buf = gdn.to_device(pack)
+    ms = _time_events(torch, lambda: gdn.prefill(h, buf, stream), stream, flush, steps=5)
+    B = algorithmic_bytes(pack.total_tokens, 16, 32, 128, 1, pack.num_ckpts)
+    entry = {"tokens": pack.total_tokens, "whole_us": ms * 1e3}
+    for parts in (3, 4):
+        seg = (pack.total_tokens + parts - 1) // parts  # rounded up to the chunk grid
+        seg = (seg + 63) // 64 * 64
+        nbytes = gdn.gdn_prefill_split_workspace_size(buf.cfg, buf.cu, buf.ckpt_cu,
+                                                      buf.ckpt_pos, seg)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=buf.o.device)
+        ms_s = _time_events(torch, lambda: gdn.gdn_prefill_packed_split(
+            h, buf.cfg, buf.cu, buf.q, buf.k, buf.v, buf.a, buf.beta, buf.init, buf.ckpt_cu,
+            buf.ckpt_pos, buf.o, buf.ckpt, buf.final, seg, ws, nbytes, stream),
+            stream, flush, steps=5)
+        entry[f"split{parts}_us"] = ms_s * 1e3
+        entry[f"split{parts}_segment"] = seg
+        del ws
+    entry["best_frac_hbm"] = B / (min(v for kk, v in entry.items() if kk.endswith("_us"))
+                                  / 1e6) / 1e9 / hbm_gbs
+    out["single_32k"] = entry
+    del buf
     # decode: 32 sequences, states resumed from a pool
     ms_step = I.mixed_step()
     B = ms_step.dec_q.shape[0]

@@ -272,6 +272,41 @@ gdn_status gdn_prefill_packed_noalloc(const gdn_config* cfg, int32_t num_seqs,
                                       void* o, float* ckpt_states, float* final_states,
                                       void* stream);
 
+/* ---- sequence splitting ------------------------------------------------------------ */
+
+/* Device workspace bytes that gdn_prefill_packed_split needs for this pack and segment
+ * length (work lists of its two passes plus fp32 scratch states: two per segment map and
+ * two per split segment). Validates what gdn_prefill_packed_split validates about the
+ * pack. Result is a multiple of 256. */
+gdn_status gdn_prefill_split_workspace_size(const gdn_config* cfg, int32_t num_seqs,
+                                            const int32_t* cu_seqlens_host,
+                                            const int32_t* ckpt_cu_host,
+                                            const int32_t* ckpt_pos_host, int32_t segment_len,
+                                            size_t* bytes);
+
+/* gdn_prefill_packed with prompts longer than `segment_len` tokens cut into segments of
+ * `segment_len` (a multiple of 64, >= 64) that run in parallel: more (segment, value head)
+ * units for packs with few prompts, such as one very long prompt. The recurrence is affine
+ * in a segment's initial state, S_end = S_start M + B; pass 1 computes, for every middle
+ * segment, B (from a zero state) and M (from the identity with v taken as zero) next to
+ * segment 0 of every prompt; a scan composes the maps in fp32 into each segment's initial
+ * state; pass 2 runs segments 1 .. P-1 from those states with their checkpoints. The work
+ * is about (2P - 1) / P times that of one pass, in about 2 / P of its sequential chunks.
+ * Arguments, layouts and errors are those of gdn_prefill_packed plus `segment_len`
+ * (INVALID_ARGUMENT when it is not a positive multiple of 64). Results equal
+ * gdn_prefill_packed's to rounding: the composed state carries the maps' fp32 rounding
+ * and the fp16 tensor-core operands of each run (the same tolerance applies). Prompts
+ * of at most `segment_len` tokens run exactly as in gdn_prefill_packed. `o` is written
+ * twice for middle segments (the first write is scratch). */
+gdn_status gdn_prefill_packed_split(gdn_handle* handle, const gdn_config* cfg,
+                                    int32_t num_seqs, const int32_t* cu_seqlens_host,
+                                    const void* q, const void* k, const void* v,
+                                    const float* a, const float* beta,
+                                    const float* initial_state, const int32_t* ckpt_cu_host,
+                                    const int32_t* ckpt_pos_host, void* o, float* ckpt_states,
+                                    float* final_states, int32_t segment_len, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
 /* ---- host-side scheduling policy (no device work) ---------------------------------- */
 
 /* Prefix-cache checkpoint position of a prompt of `len` tokens on a grid of `block`

@@ -331,18 +331,14 @@ gdn_status gdn_prefill_workspace_size(const gdn_config* cfg, int32_t num_seqs,
   return GDN_OK;
 }
 
-gdn_status gdn_prefill_packed(gdn_handle* h, const gdn_config* cfg, int32_t num_seqs,
-                              const int32_t* cu, const void* q, const void* k, const void* v,
-                              const float* a, const float* beta, const float* init,
-                              const int32_t* ckpt_cu, const int32_t* ckpt_pos, void* o,
-                              float* ckpt_states, float* final_states, void* workspace,
-                              size_t workspace_bytes, void* stream) {
-  KernelFamily fam;
-  ListLayout L;
-  int32_t num_ckpt = 0;
-  gdn_status s = plan(h, cfg, num_seqs, cu, ckpt_cu, ckpt_pos, &fam, &L, &num_ckpt);
-  if (s != GDN_OK) return s;
-  const int64_t T = cu[num_seqs];
+namespace {
+
+// Pointer, alignment and overlap checks shared by the prefill entry points.
+gdn_status check_buffers(const gdn_config* cfg, int32_t num_seqs, int64_t T, int32_t num_ckpt,
+                         const void* q, const void* k, const void* v, const float* a,
+                         const float* beta, const float* init, void* o, float* ckpt_states,
+                         float* final_states, void* workspace, size_t workspace_bytes,
+                         size_t workspace_needed) {
   const int D = cfg->head_dim_k;
   const size_t es = cfg->io_dtype == GDN_BF16 ? 2 : 4;
   if (T > 0 && (!q || !k || !v || !a || !beta || !o)) return GDN_ERR_INVALID_ARGUMENT;
@@ -353,8 +349,7 @@ gdn_status gdn_prefill_packed(gdn_handle* h, const gdn_config* cfg, int32_t num_
     if (p && !aligned16(p)) return GDN_ERR_INVALID_ARGUMENT;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
     return GDN_ERR_INVALID_ARGUMENT;
-  if (workspace_bytes < L.total) return GDN_ERR_WORKSPACE_TOO_SMALL;
-  if (!h) return GDN_ERR_INVALID_ARGUMENT;
+  if (workspace_bytes < workspace_needed) return GDN_ERR_WORKSPACE_TOO_SMALL;
 
   // outputs must not overlap each other, the inputs or the workspace (final may == init)
   const size_t state_bytes = (size_t)cfg->num_v_heads * D * D * 4;
@@ -369,7 +364,7 @@ gdn_status gdn_prefill_packed(gdn_handle* h, const gdn_config* cfg, int32_t num_
                        rng(v, (size_t)T * cfg->num_v_heads * D * es),
                        rng(a, (size_t)T * cfg->num_v_heads * 4),
                        rng(beta, (size_t)T * cfg->num_v_heads * 4),
-                       rng(workspace, L.total)};
+                       rng(workspace, workspace_needed)};
   for (int i = 0; i < 3; ++i) {
     if (outs[i].lo == 0 || outs[i].hi == outs[i].lo) continue;
     for (int j = i + 1; j < 3; ++j)
@@ -382,6 +377,60 @@ gdn_status gdn_prefill_packed(gdn_handle* h, const gdn_config* cfg, int32_t num_
     for (const Range& r : outs)
       if (r.lo && r.hi > r.lo && overlaps(ir, r)) return GDN_ERR_INVALID_ARGUMENT;
   }
+  return GDN_OK;
+}
+
+// Kernel arguments of one prefill launch over a work list at `list` (layout L).
+gdn::PrefillArgs prefill_args(const gdn_config* cfg, const ListLayout& L, char* list,
+                              int32_t* status, const void* q, const void* k, const void* v,
+                              const float* a, const float* beta, const float* init, void* o,
+                              float* ckpt_states, float* final_states) {
+  gdn::PrefillArgs pa;
+  pa.q = q; pa.k = k; pa.v = v; pa.a = a; pa.beta = beta; pa.init = init;
+  pa.o = o; pa.ckpt = ckpt_states; pa.final_state = final_states;
+  pa.units = reinterpret_cast<const GdnUnit*>(list + L.units_off);
+  pa.seqs = reinterpret_cast<const GdnSeq*>(list + L.seqs_off);
+  pa.ckpt_pos = reinterpret_cast<const int32_t*>(list + L.pos_off);
+  pa.num_units = L.num_units;
+  pa.hk_heads = cfg->num_k_heads;
+  pa.hv_heads = cfg->num_v_heads;
+  pa.group = cfg->num_v_heads / cfg->num_k_heads;
+  pa.scale = cfg->scale;
+  pa.l2norm = cfg->qk_l2norm ? 1 : 0;
+  pa.status = status;
+  pa.gate_mode = cfg->gate_mode;
+  pa.a_log = cfg->a_log;
+  pa.dt_bias = cfg->dt_bias;
+  return pa;
+}
+
+int launch_prefill(KernelFamily fam, const gdn_handle* h, const gdn_config* cfg,
+                   const gdn::PrefillArgs& pa, int64_t T, void* stream) {
+  if (fam == kChunked) {
+    const int schedule = h && h->kernel_pref >= 2 ? h->kernel_pref : gdn::kChunkedAuto;
+    return gdn::launch_chunked_prefill(pa, T, schedule, stream);
+  }
+  return gdn::launch_recurrent_prefill(pa, cfg->head_dim_k, cfg->io_dtype == GDN_BF16, stream);
+}
+
+}  // namespace
+
+gdn_status gdn_prefill_packed(gdn_handle* h, const gdn_config* cfg, int32_t num_seqs,
+                              const int32_t* cu, const void* q, const void* k, const void* v,
+                              const float* a, const float* beta, const float* init,
+                              const int32_t* ckpt_cu, const int32_t* ckpt_pos, void* o,
+                              float* ckpt_states, float* final_states, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  KernelFamily fam;
+  ListLayout L;
+  int32_t num_ckpt = 0;
+  gdn_status s = plan(h, cfg, num_seqs, cu, ckpt_cu, ckpt_pos, &fam, &L, &num_ckpt);
+  if (s != GDN_OK) return s;
+  const int64_t T = cu[num_seqs];
+  s = check_buffers(cfg, num_seqs, T, num_ckpt, q, k, v, a, beta, init, o, ckpt_states,
+                    final_states, workspace, workspace_bytes, L.total);
+  if (s != GDN_OK) return s;
+  if (!h) return GDN_ERR_INVALID_ARGUMENT;
 
   int prev = 0;
   if (cudaGetDevice(&prev) != cudaSuccess) return GDN_ERR_CUDA;
@@ -399,26 +448,236 @@ gdn_status gdn_prefill_packed(gdn_handle* h, const gdn_config* cfg, int32_t num_
   }
   if (s == GDN_OK) {
     char* ws = static_cast<char*>(workspace);
-    gdn::PrefillArgs pa;
-    pa.q = q; pa.k = k; pa.v = v; pa.a = a; pa.beta = beta; pa.init = init;
-    pa.o = o; pa.ckpt = ckpt_states; pa.final_state = final_states;
-    pa.units = reinterpret_cast<const GdnUnit*>(ws + L.units_off);
-    pa.seqs = reinterpret_cast<const GdnSeq*>(ws + L.seqs_off);
-    pa.ckpt_pos = reinterpret_cast<const int32_t*>(ws + L.pos_off);
-    pa.num_units = L.num_units;
-    pa.hk_heads = cfg->num_k_heads;
-    pa.hv_heads = cfg->num_v_heads;
-    pa.group = cfg->num_v_heads / cfg->num_k_heads;
-    pa.scale = cfg->scale;
-    pa.l2norm = cfg->qk_l2norm ? 1 : 0;
-    pa.status = reinterpret_cast<int32_t*>(ws);
-    pa.gate_mode = cfg->gate_mode;
-    pa.a_log = cfg->a_log;
-    pa.dt_bias = cfg->dt_bias;
-    const int schedule = h->kernel_pref >= 2 ? h->kernel_pref : gdn::kChunkedAuto;
-    int e = fam == kChunked ? gdn::launch_chunked_prefill(pa, T, schedule, stream)
-                            : gdn::launch_recurrent_prefill(pa, D, cfg->io_dtype == GDN_BF16,
-                                                            stream);
+    const gdn::PrefillArgs pa =
+        prefill_args(cfg, L, ws, reinterpret_cast<int32_t*>(ws), q, k, v, a, beta, init, o,
+                     ckpt_states, final_states);
+    if (launch_prefill(fam, h, cfg, pa, T, stream) != 0) s = GDN_ERR_CUDA;
+  }
+  if (prev != h->device) cudaSetDevice(prev);
+  return s;
+}
+
+// ---- sequence splitting ------------------------------------------------------------------
+
+namespace {
+
+struct VSeq {
+  int32_t tok_start, len, ckpt_begin, ckpt_end, flags;
+};
+
+// Work-list image for a list of virtual prompts (same layout and longest-first order as
+// build_worklist); ckpt positions are copied as given.
+void build_vworklist(void* dst, const ListLayout& L, KernelFamily fam, const gdn_config* c,
+                     const std::vector<VSeq>& vs, const std::vector<int32_t>& pos) {
+  std::memset(dst, 0, L.total);
+  char* base = static_cast<char*>(dst);
+  int32_t* header = reinterpret_cast<int32_t*>(base);
+  header[1] = L.num_units;
+  GdnSeq* seqs = reinterpret_cast<GdnSeq*>(base + L.seqs_off);
+  for (size_t n = 0; n < vs.size(); ++n)
+    seqs[n] = GdnSeq{vs[n].tok_start, vs[n].len, vs[n].ckpt_begin, vs[n].ckpt_end, vs[n].flags};
+  if (!pos.empty()) std::memcpy(base + L.pos_off, pos.data(), sizeof(int32_t) * pos.size());
+  std::vector<int32_t> order(vs.size());
+  for (size_t n = 0; n < vs.size(); ++n) order[n] = (int32_t)n;
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int32_t x, int32_t y) { return vs[x].len > vs[y].len; });
+  GdnUnit* units = reinterpret_cast<GdnUnit*>(base + L.units_off);
+  const int32_t per_head = units_per_head(fam, c->head_dim_v);
+  const int32_t rows = c->head_dim_v / per_head;
+  int32_t u = 0;
+  for (int32_t n : order)
+    for (int32_t h = 0; h < c->num_v_heads; ++h)
+      for (int32_t r = 0; r < per_head; ++r) units[u++] = GdnUnit{n, h, r * rows, rows};
+}
+
+// The split plan. Pass A runs, in one launch, segment 0 of every prompt from the caller's
+// initial state (unsplit prompts entirely), then for every middle segment p of a split
+// prompt B_p (zero start) and M_p (identity start, v taken as zero). The maps compose into
+// the initial states of segments 1 .. P-1, which pass C runs with their checkpoints.
+struct SplitPlan {
+  std::vector<VSeq> va, vc;
+  std::vector<int32_t> fill;    // pass A initial states: caller's prompt i, zero, identity
+  std::vector<gdn::SplitCompose> jobs;
+  std::vector<int32_t> gather;  // per prompt: final state in pass A (i) or C (-1 - i)
+  std::vector<int32_t> pos;     // checkpoint positions relative to their segment
+  ListLayout la, lc;
+  size_t off_c, off_fill, off_jobs, off_gather, host_bytes;
+  size_t off_init_a, off_fin_a, off_init_c, off_fin_c, total;
+};
+
+// `pref`: the handle's kernel preference (1 sizes for the token-serial family, which has
+// the most units).
+gdn_status plan_split(int32_t pref, const gdn_config* cfg, int32_t num_seqs, const int32_t* cu,
+                      const int32_t* ckpt_cu, const int32_t* ckpt_pos, int32_t seg,
+                      bool have_init, KernelFamily* fam, SplitPlan* sp) {
+  gdn_status s = check_config(cfg);
+  if (s != GDN_OK) return s;
+  if (seg < 64 || seg % 64 != 0) return GDN_ERR_INVALID_ARGUMENT;
+  int32_t num_ckpt = 0;
+  s = check_pack(cfg, num_seqs, cu, ckpt_cu, ckpt_pos, &num_ckpt);
+  if (s != GDN_OK) return s;
+  *fam = pref == 1 || !(gdn::kChunkedReady && chunked_supported(cfg)) ? kRecurrent : kChunked;
+  SplitPlan& P = *sp;
+  P.pos.assign(ckpt_pos ? ckpt_pos : nullptr, ckpt_pos ? ckpt_pos + num_ckpt : nullptr);
+  auto segs_of = [&](int32_t n) {
+    const int32_t len = cu[n + 1] - cu[n];
+    return len > seg ? (len + seg - 1) / seg : 1;
+  };
+  // checkpoint range [j0, j1) of prompt n inside segment p, positions made segment-relative
+  auto ckpt_range = [&](int32_t n, int32_t p, int32_t* j0, int32_t* j1) {
+    *j0 = *j1 = 0;
+    if (!ckpt_cu) return;
+    int32_t j = ckpt_cu[n];
+    while (j < ckpt_cu[n + 1] && (ckpt_pos[j] - 1) / seg < p) ++j;
+    *j0 = j;
+    while (j < ckpt_cu[n + 1] && (ckpt_pos[j] - 1) / seg == p) {
+      P.pos[j] = ckpt_pos[j] - p * seg;
+      ++j;
+    }
+    *j1 = j;
+  };
+  // pass A: segment 0 of every prompt (index n), then the maps of split prompts
+  for (int32_t n = 0; n < num_seqs; ++n) {
+    const int32_t len = cu[n + 1] - cu[n];
+    int32_t j0, j1;
+    ckpt_range(n, 0, &j0, &j1);
+    P.va.push_back(VSeq{cu[n], std::min(len, seg), j0, j1, 0});
+    P.fill.push_back(have_init ? n : gdn::kSplitZero);
+  }
+  for (int32_t n = 0; n < num_seqs; ++n) {
+    const int32_t np = segs_of(n);
+    if (np == 1) {
+      P.gather.push_back(n);
+      continue;
+    }
+    gdn::SplitCompose job;
+    job.num_segments = np;
+    job.first_final = n;
+    job.first_map = (int32_t)P.va.size();
+    job.first_init = (int32_t)P.vc.size();
+    for (int32_t p = 1; p + 1 < np; ++p) {
+      P.va.push_back(VSeq{cu[n] + p * seg, seg, 0, 0, 0});                // B_p
+      P.fill.push_back(gdn::kSplitZero);
+      P.va.push_back(VSeq{cu[n] + p * seg, seg, 0, 0, gdn::kSeqZeroV});   // M_p
+      P.fill.push_back(gdn::kSplitIdentity);
+    }
+    for (int32_t p = 1; p < np; ++p) {
+      int32_t j0, j1;
+      ckpt_range(n, p, &j0, &j1);
+      P.vc.push_back(VSeq{cu[n] + p * seg, std::min(seg, cu[n + 1] - cu[n] - p * seg), j0, j1,
+                          0});
+    }
+    P.gather.push_back(-1 - (int32_t)(P.vc.size() - 1));
+    P.jobs.push_back(job);
+  }
+  const int32_t per_head = units_per_head(*fam, cfg->head_dim_v);
+  const int64_t ua = (int64_t)P.va.size() * cfg->num_v_heads * per_head;
+  const int64_t uc = (int64_t)P.vc.size() * cfg->num_v_heads * per_head;
+  if (ua > INT32_MAX || uc > INT32_MAX) return GDN_ERR_UNSUPPORTED;
+  P.la = layout_for((int32_t)P.va.size(), (int32_t)ua, num_ckpt);
+  P.lc = layout_for(std::max<int32_t>((int32_t)P.vc.size(), 1), (int32_t)uc, num_ckpt);
+  P.off_c = P.la.total;
+  P.off_fill = align_up(P.off_c + P.lc.total, kAlign);
+  P.off_jobs = align_up(P.off_fill + sizeof(int32_t) * P.fill.size(), kAlign);
+  P.off_gather = align_up(
+      P.off_jobs + sizeof(gdn::SplitCompose) * std::max<size_t>(P.jobs.size(), 1), kAlign);
+  P.host_bytes = align_up(P.off_gather + sizeof(int32_t) * P.gather.size(), kAlign);
+  const size_t sb = (size_t)cfg->num_v_heads * cfg->head_dim_v * cfg->head_dim_k * 4;
+  P.off_init_a = P.host_bytes;
+  P.off_fin_a = align_up(P.off_init_a + sb * P.va.size(), kAlign);
+  P.off_init_c = align_up(P.off_fin_a + sb * P.va.size(), kAlign);
+  P.off_fin_c = align_up(P.off_init_c + sb * P.vc.size(), kAlign);
+  P.total = align_up(P.off_fin_c + sb * P.vc.size(), kAlign);
+  return GDN_OK;
+}
+
+}  // namespace
+
+gdn_status gdn_prefill_split_workspace_size(const gdn_config* cfg, int32_t num_seqs,
+                                            const int32_t* cu_seqlens_host,
+                                            const int32_t* ckpt_cu_host,
+                                            const int32_t* ckpt_pos_host, int32_t segment_len,
+                                            size_t* bytes) {
+  if (!bytes) return GDN_ERR_INVALID_ARGUMENT;
+  KernelFamily fam;
+  SplitPlan sp;
+  // sized for the family with the most units, so the answer does not depend on a handle
+  const gdn_status s = plan_split(1, cfg, num_seqs, cu_seqlens_host, ckpt_cu_host,
+                                  ckpt_pos_host, segment_len, true, &fam, &sp);
+  if (s != GDN_OK) return s;
+  *bytes = sp.total;
+  return GDN_OK;
+}
+
+gdn_status gdn_prefill_packed_split(gdn_handle* h, const gdn_config* cfg, int32_t num_seqs,
+                                    const int32_t* cu, const void* q, const void* k,
+                                    const void* v, const float* a, const float* beta,
+                                    const float* init, const int32_t* ckpt_cu,
+                                    const int32_t* ckpt_pos, void* o, float* ckpt_states,
+                                    float* final_states, int32_t segment_len, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  KernelFamily fam;
+  SplitPlan P;
+  gdn_status s = plan_split(h ? h->kernel_pref : 0, cfg, num_seqs, cu, ckpt_cu, ckpt_pos,
+                            segment_len, init != nullptr, &fam, &P);
+  if (s != GDN_OK) return s;
+  const int64_t T = cu[num_seqs];
+  const int32_t num_ckpt = ckpt_cu ? ckpt_cu[num_seqs] : 0;
+  s = check_buffers(cfg, num_seqs, T, num_ckpt, q, k, v, a, beta, init, o, ckpt_states,
+                    final_states, workspace, workspace_bytes, P.total);
+  if (s != GDN_OK) return s;
+  if (!h) return GDN_ERR_INVALID_ARGUMENT;
+
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (prev != h->device && cudaSetDevice(h->device) != cudaSuccess) return GDN_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  const int hv = cfg->num_v_heads, d = cfg->head_dim_v;
+  float* init_a = reinterpret_cast<float*>(ws + P.off_init_a);
+  float* fin_a = reinterpret_cast<float*>(ws + P.off_fin_a);
+  float* init_c = reinterpret_cast<float*>(ws + P.off_init_c);
+  float* fin_c = reinterpret_cast<float*>(ws + P.off_fin_c);
+
+  StagingSlot* slot = nullptr;
+  s = take_slot(h, P.host_bytes, &slot);
+  if (s == GDN_OK) {
+    char* img = static_cast<char*>(slot->host);
+    build_vworklist(img, P.la, fam, cfg, P.va, P.pos);
+    build_vworklist(img + P.off_c, P.lc, fam, cfg, P.vc, P.pos);
+    std::memcpy(img + P.off_fill, P.fill.data(), sizeof(int32_t) * P.fill.size());
+    if (!P.jobs.empty())
+      std::memcpy(img + P.off_jobs, P.jobs.data(), sizeof(gdn::SplitCompose) * P.jobs.size());
+    std::memcpy(img + P.off_gather, P.gather.data(), sizeof(int32_t) * P.gather.size());
+    cudaError_t e = cudaMemcpyAsync(ws, img, P.host_bytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaEventRecord(slot->done, st);
+    slot->used = true;
+    if (e != cudaSuccess) s = GDN_ERR_CUDA;
+  }
+  int e = 0;
+  if (s == GDN_OK) {
+    // pass A: segment 0 of every prompt and the segment maps of split prompts
+    e = gdn::launch_fill_states(init_a, init, reinterpret_cast<const int32_t*>(ws + P.off_fill),
+                                (int)P.va.size(), hv, d, stream);
+    if (e == 0)
+      e = launch_prefill(fam, h, cfg,
+                         prefill_args(cfg, P.la, ws, status, q, k, v, a, beta, init_a, o,
+                                      ckpt_states, fin_a),
+                         T, stream);
+    // the initial states of segments 1 .. P-1, then pass C
+    if (e == 0)
+      e = gdn::launch_compose_maps(reinterpret_cast<const gdn::SplitCompose*>(ws + P.off_jobs),
+                                   (int)P.jobs.size(), fin_a, init_c, hv, d, stream);
+    if (e == 0 && !P.vc.empty())
+      e = launch_prefill(fam, h, cfg,
+                         prefill_args(cfg, P.lc, ws + P.off_c, status, q, k, v, a, beta, init_c,
+                                      o, ckpt_states, fin_c),
+                         T, stream);
+    if (e == 0)
+      e = gdn::launch_gather_states(final_states, fin_a, fin_c,
+                                    reinterpret_cast<const int32_t*>(ws + P.off_gather),
+                                    num_seqs, hv, d, stream);
     if (e != 0) s = GDN_ERR_CUDA;
   }
   if (prev != h->device) cudaSetDevice(prev);

@@ -321,7 +321,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       prefetch_tmap(&P.tk);
       prefetch_tmap(&P.tv);
       issue_kq(P, sKQ, &sm.bar_kq, hk, sd.tok_start);
-      issue_v(P, sV, &sm.bar_v, h, sd.tok_start);
+      if (!(sd.flags & kSeqZeroV)) issue_v(P, sV, &sm.bar_v, h, sd.tok_start);
     }
   }
   if (warp == 0) {
@@ -372,7 +372,8 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
 
   uint32_t ph_mma = 0, ph_kq = 0, ph_v = 0;
   bool ok = true;
-  bool kq_inflight = nchunks > 0, v_inflight = nchunks > 0;  // meaningful in thread 0
+  const bool vz = sd.flags & kSeqZeroV;  // v taken as zero: no v copies at all
+  bool kq_inflight = nchunks > 0, v_inflight = nchunks > 0 && !vz;  // meaningful in thread 0
   int c_next = sd.ckpt_begin;
   const float scale = p.scale;
 
@@ -410,8 +411,10 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
     // ---- (2) wait for q, k, v; convert in place to fp16 (q, k normalised); zero past L ----
     if (!(ok = wait_all(&sm.bar_kq, ph_kq))) break;
     kq_inflight = false;
-    if (!(ok = wait_all(&sm.bar_v, ph_v))) break;
-    v_inflight = false;
+    if (!vz) {
+      if (!(ok = wait_all(&sm.bar_v, ph_v))) break;
+      v_inflight = false;
+    }
     if (tid == 0 && c + 1 < nchunks) {  // warm L2 with the next chunk's q, k, v
       const int nrow = sd.tok_start + t0 + kC;
 #pragma unroll
@@ -503,7 +506,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
         const uint32_t r = pass * 16 + rsub;
         *reinterpret_cast<uint4*>(sV + reg * 8192 + (r >> 3) * 1024 + (r & 7) * 128 +
                                   ((cc ^ (r & 7)) << 4)) =
-            (int)r < L ? bf16x8_to_half8(w[pass]) : zero;
+            (int)r < L && !vz ? bf16x8_to_half8(w[pass]) : zero;
       }
     }
     if (!(ok = wait_all(&sm.bar_mma, ph_mma))) break;
@@ -645,7 +648,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
     __syncwarp();
     if (!(ok = wait_all(&sm.bar_mma, ph_mma))) break;
     // V and T2 are consumed: fetch the next chunk's v now
-    if (tid == 0 && c + 1 < nchunks) {
+    if (tid == 0 && c + 1 < nchunks && !vz) {
       issue_v(P, sV, &sm.bar_v, h, sd.tok_start + t0 + kC);
       v_inflight = true;
     }

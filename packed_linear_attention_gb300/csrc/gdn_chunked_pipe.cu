@@ -510,7 +510,7 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
       prefetch_tmap(&P.tk);
       prefetch_tmap(&P.tv);
       issue_kq(P, sm, smem + OFF_KQ, 0, hk, sd.tok_start);
-      issue_v(P, sm, sV, h, sd.tok_start);
+      if (!(sd.flags & kSeqZeroV)) issue_v(P, sm, sV, h, sd.tok_start);
       if (nchunks > 1) issue_kq(P, sm, smem + OFF_KQ + kKQW, 1, hk, sd.tok_start + kC);
     }
   }
@@ -667,7 +667,8 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
       __syncwarp();
       if (!(ok = group_wait(sm, B_M2, c & 1, kBarPrep, leader))) break;
       // V is consumed: fetch the next chunk's
-      if (leader && c + 1 < nchunks) issue_v(P, sm, sV, h, sd.tok_start + t0 + kC);
+      if (leader && c + 1 < nchunks && !(sd.flags & kSeqZeroV))
+        issue_v(P, sm, sV, h, sd.tok_start + t0 + kC);
 
       // ---- (8) -W -> rows 128-191 of the q/k/w tile (fp16, K-major: rows tokens); hand over ---
       {
@@ -732,9 +733,15 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
       return true;
     };
     // Stages chunk cc's v (copied by the prep group once the previous v was consumed).
+    // (v taken as zero: the tile is zeroed once and never copied into)
     auto stage_v = [&](int cc) -> bool {
-      if (!group_wait(sm, B_V, cc & 1, kBarChain, leader)) return false;
-      convert_v(sV, min(kC, sd.len - cc * kC), ctid);
+      if (!(sd.flags & kSeqZeroV)) {
+        if (!group_wait(sm, B_V, cc & 1, kBarChain, leader)) return false;
+        convert_v(sV, min(kC, sd.len - cc * kC), ctid);
+      } else if (cc == 0) {
+        for (int i = ctid; i < 1024; i += kGroup)
+          reinterpret_cast<uint4*>(sV)[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
       fence_proxy_async_smem();
       named_sync(kBarChain, kGroup);
       if (leader) mbar_arrive(&sm.bar[B_VCONV]);

@@ -30,7 +30,9 @@ struct GdnSeq {
   int32_t len;         // tokens in the prompt's segment
   int32_t ckpt_begin;  // CSR range of this prompt's checkpoints
   int32_t ckpt_end;
+  int32_t flags;       // kSeqZeroV: v is taken as zero (sequence splitting's map runs)
 };
+constexpr int32_t kSeqZeroV = 1;
 
 // Everything a prefill kernel needs besides the work list.
 struct PrefillArgs {
@@ -117,6 +119,23 @@ int launch_chunked_prefill(const PrefillArgs& a, int64_t total_tokens, int sched
 // q, k (H_k * d columns) and v (H_v * d columns) with total_tokens rows (gdn_tma.cu).
 bool make_qkv_maps(const PrefillArgs& a, int64_t total_tokens, int head_dim, CUtensorMap* tq,
                    CUtensorMap* tk, CUtensorMap* tv);
+
+// Sequence splitting (gdn_split.cu). fill_states modes besides "copy the caller's state of
+// prompt i" (i >= 0):
+constexpr int32_t kSplitZero = -1, kSplitIdentity = -2;
+// One split prompt: its segment-0 final state is finals_a[first_final]; B_p and M_p of
+// segments p = 1 .. num_segments - 2 are finals_a[first_map + 2 (p - 1)] and the one after;
+// the initial state of segment p >= 1 goes to inits_c[first_init + p - 1].
+struct SplitCompose {
+  int32_t num_segments, first_final, first_map, first_init;
+};
+int launch_fill_states(float* dst, const float* src, const int32_t* mode, int count, int hv,
+                       int d, void* stream);
+int launch_compose_maps(const SplitCompose* jobs, int num_jobs, const float* finals_a,
+                        float* inits_c, int hv, int d, void* stream);
+// dst[n] = index[n] >= 0 ? src_a[index[n]] : src_c[-1 - index[n]] (per prompt, all heads)
+int launch_gather_states(float* dst, const float* src_a, const float* src_c,
+                         const int32_t* index, int num_seqs, int hv, int d, void* stream);
 
 // Host-side planning shared with the allocation-free entry point (gdn_noalloc.cu):
 // the kernel family, the work-list layout and its size for one pack.

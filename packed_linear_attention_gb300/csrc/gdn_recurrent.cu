@@ -105,7 +105,8 @@ recurrent_prefill_kernel(PrefillArgs p) {
         sk[j][lane + 32 * e] = kv[e] * ks;
       }
       if (u.row0 + lane < u.row0 + u.nrows)
-        sv[j][lane] = to_f32(v[(tok * p.hv_heads + h) * D + u.row0 + lane]);
+        sv[j][lane] = (sd.flags & kSeqZeroV) ? 0.f
+                                              : to_f32(v[(tok * p.hv_heads + h) * D + u.row0 + lane]);
       if (lane == 0) {
         float a = p.a[tok * p.hv_heads + h], b = p.beta[tok * p.hv_heads + h];
         if (p.gate_mode == 1) gate_from_raw(p.a_log[h], p.dt_bias[h], a, b);

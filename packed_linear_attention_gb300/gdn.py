@@ -43,7 +43,8 @@ EXPORTS = (
     "gdn_checkpoint_copy_query", "gdn_checkpoint_copy_wait", "gdn_decode_step",
     "gdn_ckpt_position", "gdn_mixed_budget", "gdn_prefill_worklist_host",
     "gdn_prefill_packed_noalloc", "gdn_prefill_packed_async", "gdn_prefill_async_query",
-    "gdn_prefill_async_wait", "gdn_prefill_async_join",
+    "gdn_prefill_async_wait", "gdn_prefill_async_join", "gdn_prefill_split_workspace_size",
+    "gdn_prefill_packed_split",
 )
 
 
@@ -89,6 +90,10 @@ def load(path: str = LIB_PATH):
             "gdn_prefill_workspace_size": (I32, [CFG, I32, IP, IP, ctypes.POINTER(SZ)]),
             "gdn_prefill_packed": (I32, [P, CFG, I32, IP, P, P, P, P, P, P, IP, IP, P, P, P,
                                          P, SZ, P]),
+            "gdn_prefill_split_workspace_size": (I32, [CFG, I32, IP, IP, IP, I32,
+                                                       ctypes.POINTER(ctypes.c_size_t)]),
+            "gdn_prefill_packed_split": (I32, [P, CFG, I32, IP, P, P, P, P, P, P, IP, IP, P, P,
+                                               P, I32, P, SZ, P]),
             "gdn_read_device_status": (I32, [P, IP, P]),
             "gdn_prefill_packed_noalloc": (I32, [CFG, I32, IP, P, P, P, P, P, P, IP, IP, P, P,
                                                  P, P]),
@@ -208,6 +213,31 @@ def gdn_prefill_packed(handle, cfg, cu_seqlens, q, k, v, a, beta, initial_state,
     return st
 
 
+def gdn_prefill_split_workspace_size(cfg: gdn_config, cu_seqlens, ckpt_cu=None, ckpt_pos=None,
+                                     segment_len: int = 4096) -> int:
+    n = ctypes.c_size_t()
+    _check(load().gdn_prefill_split_workspace_size(ctypes.byref(cfg), len(cu_seqlens) - 1,
+                                                   _i32(cu_seqlens), _i32(ckpt_cu),
+                                                   _i32(ckpt_pos), int(segment_len),
+                                                   ctypes.byref(n)),
+           "gdn_prefill_split_workspace_size")
+    return n.value
+
+
+def gdn_prefill_packed_split(handle, cfg, cu_seqlens, q, k, v, a, beta, initial_state, ckpt_cu,
+                             ckpt_pos, o, ckpt_states, final_states, segment_len, workspace,
+                             workspace_bytes, stream=None, *, raise_on_error=True) -> int:
+    """gdn_prefill_packed with prompts longer than segment_len cut into parallel segments."""
+    st = load().gdn_prefill_packed_split(
+        handle, ctypes.byref(cfg), len(cu_seqlens) - 1, _i32(cu_seqlens), _addr(q), _addr(k),
+        _addr(v), _addr(a), _addr(beta), _addr(initial_state), _i32(ckpt_cu), _i32(ckpt_pos),
+        _addr(o), _addr(ckpt_states), _addr(final_states), int(segment_len), _addr(workspace),
+        int(workspace_bytes), _stream(stream))
+    if raise_on_error:
+        _check(st, "gdn_prefill_packed_split")
+    return st
+
+
 def gdn_prefill_packed_noalloc(cfg, cu_seqlens, q, k, v, a, beta, initial_state, ckpt_cu,
                                ckpt_pos, o, ckpt_states, final_states, stream=None, *,
                                raise_on_error=True) -> int:
@@ -255,6 +285,21 @@ def gdn_prefill_async_join(handle, stream=None) -> None:
     _check(load().gdn_prefill_async_join(handle, _stream(stream)), "gdn_prefill_async_join")
 
 
+def prefill_split(handle, buf: "DeviceBuffers", segment_len: int, stream=None) -> int:
+    """gdn_prefill_packed_split on a DeviceBuffers bundle (allocates its own workspace)."""
+    import torch
+    ckpt_pos = buf.ckpt_pos if len(buf.ckpt_pos) else None
+    nbytes = gdn_prefill_split_workspace_size(buf.cfg, buf.cu, buf.ckpt_cu, ckpt_pos,
+                                              segment_len)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=buf.o.device)
+    st = gdn_prefill_packed_split(handle, buf.cfg, buf.cu, buf.q, buf.k, buf.v, buf.a, buf.beta,
+                                  buf.init, buf.ckpt_cu, ckpt_pos, buf.o,
+                                  buf.ckpt if buf.ckpt.numel() else None, buf.final,
+                                  segment_len, ws, nbytes, stream)
+    buf.split_workspace = ws  # keep alive until the work on the stream is done
+    return st
+
+
 def prefill_async(handle, buf: "DeviceBuffers", after_stream=None, *, raise_on_error=True) -> int:
     """gdn_prefill_packed_async on a DeviceBuffers bundle."""
     return gdn_prefill_packed_async(handle, buf.cfg, buf.cu, buf.q, buf.k, buf.v, buf.a,
@@ -280,11 +325,11 @@ def gdn_prefill_worklist_host(handle, cfg, cu_seqlens, ckpt_cu=None, ckpt_pos=No
     nu = int(raw[1])
     units_off = 256 // 4
     seqs_off = ((256 + 16 * nu + 255) // 256 * 256) // 4
-    pos_off = ((seqs_off * 4 + 16 * num_seqs + 255) // 256 * 256) // 4
+    pos_off = ((seqs_off * 4 + 20 * num_seqs + 255) // 256 * 256) // 4  # GdnSeq: 5 int32
     nck = 0 if ckpt_cu is None else int(np.asarray(ckpt_cu)[-1])
     return dict(status=int(raw[0]), num_units=nu,
                 units=raw[units_off:units_off + 4 * nu].reshape(nu, 4).copy(),
-                seqs=raw[seqs_off:seqs_off + 4 * num_seqs].reshape(num_seqs, 4).copy(),
+                seqs=raw[seqs_off:seqs_off + 5 * num_seqs].reshape(num_seqs, 5).copy(),
                 ckpt_pos=raw[pos_off:pos_off + nck].copy(), nbytes=need.value)
 
 
@@ -361,6 +406,7 @@ class DeviceBuffers:
     workspace_bytes: int
     a_log: object = None       # device tensors kept alive for the config's pointers
     dt_bias: object = None
+    split_workspace: object = None  # workspace of the last prefill_split call
 
 
 def to_device(pack, device="cuda", cfg: gdn_config | None = None) -> DeviceBuffers:

@@ -230,6 +230,15 @@ def long_prompts(num_prompts: int = 4, length: int = 8192, seed: int = 0) -> Pac
                      name=f"long_{num_prompts}x{length}")
 
 
+def single_long_prompt(length: int = 32768, seed: int = 0) -> Pack:
+    """One long-context prompt (32,768 tokens at the wave's dims, slow decay as for the 8K
+    prompts, checkpoints every 8,192 tokens): the shape where N H_v = 32 units leave most
+    SMs idle, for sequence splitting."""
+    return make_pack([length], **WAVE_HEADS, io_dtype="bf16", seed=seed,
+                     decay_scale=LONG_DECAY_SCALE, ckpt_lists=every_block([length], 8192),
+                     name="single_long_prompt")
+
+
 def mixed_budget(remaining, budget: int = 1024, max_prompts: int = 8) -> list[int]:
     """Oldest-first split of a prompt-token budget (sparkinfer v0.6.4, "What changed")."""
     take, left = [], budget
