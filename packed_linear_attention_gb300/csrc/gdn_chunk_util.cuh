@@ -1,0 +1,118 @@
+// gdn_chunk_util.cuh — device helpers shared by the two schedules of the chunked prefill
+// kernel (gdn_chunked.cu, gdn_chunked_pipe.cu): fp16 packing into 128B-swizzled operand
+// tiles, the bf16 -> fp16 widening of q/k/v, the gate loads of a chunk and the warp-level
+// tf32 tile products of the 64 x 64 triangular inverse.
+#pragma once
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "gdn_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace gdn {
+namespace chunk {
+
+constexpr int kC = 64;          // tokens per chunk
+constexpr int kD = 128;         // head dim
+constexpr int kLd = 68;         // fp32 64x64 matrix row stride (conflict-free float4 rows)
+constexpr int kLdX = 36;        // row stride of the 32 x 32 merge scratch
+constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr int kStatusTimeout = 5;  // GDN_ERR_DEVICE_TIMEOUT
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Eight fp32 values as fp16 into one 16-byte chunk of a 128B-swizzled tile.
+__device__ __forceinline__ void st_chunk(uint8_t* tile, uint32_t row, uint32_t col,
+                                         uint32_t rows_per_region, const float (&x)[8]) {
+  uint4 v;
+  v.x = pack_half2(x[0], x[1]);
+  v.y = pack_half2(x[2], x[3]);
+  v.z = pack_half2(x[4], x[5]);
+  v.w = pack_half2(x[6], x[7]);
+  *reinterpret_cast<uint4*>(tile + ptx::sw128_offset(row, col, rows_per_region)) = v;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& w, float (&x)[8]) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(u[i] << 16);
+    x[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+}
+
+// bf16 -> fp16 is exact for magnitudes in [2^-17, 65504] (8 significant bits fit in 11).
+__device__ __forceinline__ uint4 bf16x8_to_half8(const uint4& w) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 hh = __floats2half2_rn(__uint_as_float(u[i] << 16),
+                                         __uint_as_float(u[i] & 0xFFFF0000u));
+    o[i] = *reinterpret_cast<const uint32_t*>(&hh);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ uint4 pack_half8(const float (&x)[8]) {
+  return make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]),
+                    pack_half2(x[6], x[7]));
+}
+
+// Starts the loads of the log-decays and betas of the chunk at token t0 (one warp, two
+// tokens per lane). Token indices are clamped into the prompt so that nothing waits on the
+// loads here; gates_of() masks the tokens past the chunk when the values are used.
+__device__ __forceinline__ void fetch_gates(const float* ag, const float* bg, size_t stride,
+                                            int t0, int len, int lane, float (&g)[4]) {
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const size_t t = (size_t)min(t0 + lane + 32 * hh, len - 1);
+    g[hh] = __ldg(ag + t * stride);
+    g[2 + hh] = __ldg(bg + t * stride);
+  }
+}
+
+// Gates of the chunk at t0 from fetch_gates' values: raw inputs are transformed, and
+// tokens past the chunk get a = beta = 0.
+__device__ __forceinline__ void gates_of(const float (&raw_g)[4], int t0, int len, int lane,
+                                         bool raw, float a_log, float dt_bias, float (&g)[4]) {
+  const int L = min(kC, len - t0);
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    float a = raw_g[hh], b = raw_g[2 + hh];
+    if (raw) gate_from_raw(a_log, dt_bias, a, b);
+    const bool live = lane + 32 * hh < L;
+    g[hh] = live ? a : 0.f;
+    g[2 + hh] = live ? b : 0.f;
+  }
+}
+
+// One 16 x 8 output tile D = sum_k Ablk[r0.., k] * Bblk[k.., n0..] over k in [k_lo, k_hi)
+// (multiples of 8) on one warp, tf32 warp MMAs. Both matrices fp32 with row strides lda/ldb.
+__device__ __forceinline__ void tile_mm(float (&d)[4], const float* Am, int lda, int r0,
+                                        const float* Bm, int ldb, int n0, int k_lo, int k_hi,
+                                        int gid, int tig) {
+  for (int k = k_lo; k < k_hi; k += 8) {
+    const float a[4] = {Am[(r0 + gid) * lda + k + tig], Am[(r0 + gid + 8) * lda + k + tig],
+                        Am[(r0 + gid) * lda + k + tig + 4], Am[(r0 + gid + 8) * lda + k + tig + 4]};
+    const float b[2] = {Bm[(k + tig) * ldb + n0 + gid], Bm[(k + tig + 4) * ldb + n0 + gid]};
+    ptx::mma_tf32_f(d, a, b);
+  }
+}
+
+// Stores a 16 x 8 accumulator tile (optionally negated) at (r0, n0) of an fp32 matrix.
+__device__ __forceinline__ void tile_store(float* M, int ld, int r0, int n0, const float (&d)[4],
+                                           float sign, int gid, int tig) {
+  M[(r0 + gid) * ld + n0 + 2 * tig] = sign * d[0];
+  M[(r0 + gid) * ld + n0 + 2 * tig + 1] = sign * d[1];
+  M[(r0 + gid + 8) * ld + n0 + 2 * tig] = sign * d[2];
+  M[(r0 + gid + 8) * ld + n0 + 2 * tig + 1] = sign * d[3];
+}
+
+}  // namespace chunk
+}  // namespace gdn

@@ -39,20 +39,16 @@
 #include <cstdint>
 
 #include "gdn_internal.h"
+#include "gdn_chunk_util.cuh"
 #include "ptx_sm103.cuh"
 
 namespace gdn {
 namespace {
 
 using namespace ptx;
+using namespace chunk;
 
-constexpr int kC = 64;          // chunk
-constexpr int kD = 128;         // head dim
 constexpr int kThreads = 256;
-constexpr uint32_t kWaitLimit = 1u << 24;
-constexpr int kStatusTimeout = 5;  // GDN_ERR_DEVICE_TIMEOUT
-constexpr int kLd = 68;          // fp32 64x64 matrix row stride (conflict-free float4 rows)
-constexpr float kLog2e = 1.4426950408889634f;
 
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_KQ = 0;         // K (rows 0-63) and Q (rows 64-127): 2 regions x 16 KB
@@ -79,58 +75,6 @@ struct __align__(8) Smem {
   uint32_t tmem_base;
   float next_decay;  // e^{G_L} of the next chunk
 };
-
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-__device__ __forceinline__ void st_chunk(uint8_t* tile, uint32_t row, uint32_t col,
-                                         uint32_t rows_per_region, const float (&x)[8]) {
-  uint4 v;
-  v.x = pack_half2(x[0], x[1]);
-  v.y = pack_half2(x[2], x[3]);
-  v.z = pack_half2(x[4], x[5]);
-  v.w = pack_half2(x[6], x[7]);
-  *reinterpret_cast<uint4*>(tile + sw128_offset(row, col, rows_per_region)) = v;
-}
-
-__device__ __forceinline__ void unpack_bf16x8(const uint4& w, float (&x)[8]) {
-  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = __uint_as_float(u[i] << 16);
-    x[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
-  }
-}
-
-__device__ __forceinline__ void unpack_half8(const uint4& w, float (&x)[8]) {
-  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
-    x[2 * i] = f.x;
-    x[2 * i + 1] = f.y;
-  }
-}
-
-// bf16 -> fp16 is exact for magnitudes in [2^-17, 65504] (8 significant bits fit in 11).
-__device__ __forceinline__ uint4 bf16x8_to_half8(const uint4& w) {
-  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-  uint32_t o[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __half2 hh = __floats2half2_rn(__uint_as_float(u[i] << 16),
-                                         __uint_as_float(u[i] & 0xFFFF0000u));
-    o[i] = *reinterpret_cast<const uint32_t*>(&hh);
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-__device__ __forceinline__ uint4 pack_half8(const float (&x)[8]) {
-  return make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]),
-                    pack_half2(x[6], x[7]));
-}
 
 // Wait for an mbarrier phase, uniformly across the block; false on timeout.
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t& phase) {
@@ -165,6 +109,7 @@ __device__ __forceinline__ void issue_v(const ChunkedParams& P, uint8_t* sV, uin
   tma_load_2d(sV + 8192, &P.tv, h * kD + 64, row, bar);
 }
 
+
 // Loads the log-decays and betas of the chunk starting at token t0 (warp 0 only); with raw
 // gate inputs they are turned into gates here. Tokens past the chunk get a = beta = 0.
 __device__ __forceinline__ void load_gates(const float* ag, const float* bg, size_t stride,
@@ -184,30 +129,6 @@ __device__ __forceinline__ void load_gates(const float* ag, const float* bg, siz
     g[2 + hh] = b;
   }
 }
-
-// One 16 x 8 output tile D = sum_k Ablk[r0.., k] * Bblk[k.., n0..] over k in [k_lo, k_hi)
-// (multiples of 8) on one warp, tf32 warp MMAs. Both matrices fp32 with row strides lda/ldb.
-__device__ __forceinline__ void tile_mm(float (&d)[4], const float* Am, int lda, int r0,
-                                        const float* Bm, int ldb, int n0, int k_lo, int k_hi,
-                                        int gid, int tig) {
-  for (int k = k_lo; k < k_hi; k += 8) {
-    const float a[4] = {Am[(r0 + gid) * lda + k + tig], Am[(r0 + gid + 8) * lda + k + tig],
-                        Am[(r0 + gid) * lda + k + tig + 4], Am[(r0 + gid + 8) * lda + k + tig + 4]};
-    const float b[2] = {Bm[(k + tig) * ldb + n0 + gid], Bm[(k + tig + 4) * ldb + n0 + gid]};
-    mma_tf32_f(d, a, b);
-  }
-}
-
-// Stores a 16 x 8 accumulator tile (optionally negated) at (r0, n0) of an fp32 matrix.
-__device__ __forceinline__ void tile_store(float* M, int ld, int r0, int n0, const float (&d)[4],
-                                           float sign, int gid, int tig) {
-  M[(r0 + gid) * ld + n0 + 2 * tig] = sign * d[0];
-  M[(r0 + gid) * ld + n0 + 2 * tig + 1] = sign * d[1];
-  M[(r0 + gid + 8) * ld + n0 + 2 * tig] = sign * d[2];
-  M[(r0 + gid + 8) * ld + n0 + 2 * tig + 1] = sign * d[3];
-}
-
-constexpr int kLdX = 36;  // row stride of the 32 x 32 merge scratch
 
 // (I + A)^-1 for a 64 x 64 strictly-lower A (fp32, row stride kLd) into T (same stride):
 //  1. (invert_diag_blocks) the four 16 x 16 diagonal blocks by right-looking forward
