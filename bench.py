@@ -442,28 +442,32 @@ def run_secondary(torch, gdn, I, h, stream, flush, hbm_gbs):
 
 
 def run_e2e(args, torch, gdn, h, buf, pack, stream, world, dev):
-    """Host-resident inputs: per step, pinned H2D of q, k, v, a, beta, the prefill call,
-    D2H of o and the final states into pinned memory, and the checkpoint copy into the
-    handle's pinned snapshot pool on its side stream."""
+    """Host-resident inputs and outputs through gdn_prefill_packed_host: per step, the pinned
+    q, k, v, a, beta go in and o, the checkpoints and the final states come back, group by
+    group of prompts, the copies of one group overlapping the prefill of its neighbours."""
     host = {}
     for name in ("q", "k", "v", "a", "beta"):
-        t = getattr(buf, name)
-        host[name] = t.cpu().pin_memory()
+        host[name] = getattr(buf, name).cpu().pin_memory()
     o_host = torch.empty(buf.o.shape, dtype=buf.o.dtype).pin_memory()
     f_host = torch.empty(buf.final.shape, dtype=torch.float32).pin_memory()
+    c_host = torch.empty(buf.ckpt.shape, dtype=torch.float32).pin_memory()
+    has_ck = buf.ckpt.numel() > 0
+    hb = gdn.prefill_buffers(host["q"], host["k"], host["v"], host["a"], host["beta"], None,
+                             o_host, c_host if has_ck else None, f_host)
+    db = gdn.prefill_buffers(buf.q, buf.k, buf.v, buf.a, buf.beta, None, buf.o,
+                             buf.ckpt if has_ck else None, buf.final)
     h2d = sum(x.numel() * x.element_size() for x in host.values())
-    ck_bytes = buf.ckpt.numel() * 4
-    d2h = o_host.numel() * o_host.element_size() + f_host.numel() * 4 + ck_bytes
+    d2h = (o_host.numel() * o_host.element_size() + f_host.numel() * 4
+           + (c_host.numel() * 4 if has_ck else 0))
+
+    ws_bytes = gdn.gdn_prefill_host_workspace_size(buf.cfg, buf.cu, buf.ckpt_cu, args.e2e_group)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
     def step():
-        for name, t in host.items():
-            getattr(buf, name).copy_(t, non_blocking=True)
-        gdn.prefill(h, buf, stream)
-        gdn.gdn_checkpoint_copy(h, buf.ckpt, ck_bytes, 0, stream)
-        o_host.copy_(buf.o, non_blocking=True)
-        f_host.copy_(buf.final, non_blocking=True)
-        torch.cuda.synchronize()
-        gdn.gdn_checkpoint_copy_wait(h)
+        gdn.gdn_prefill_packed_host(h, buf.cfg, buf.cu, buf.ckpt_cu,
+                                    buf.ckpt_pos if has_ck else None, hb, db,
+                                    args.e2e_group, ws, ws_bytes, stream)
+        stream.synchronize()
 
     for _ in range(2):
         step()
@@ -475,7 +479,8 @@ def run_e2e(args, torch, gdn, h, buf, pack, stream, world, dev):
     dt = (time.perf_counter() - t0) / steps
     dt = reduce_max(dt, world, dev)
     return {"value": pack.total_tokens * world / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "steps": steps}
+            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "steps": steps,
+            "api": f"gdn_prefill_packed_host, groups of {args.e2e_group} prompts"}
 
 
 def main():
@@ -488,6 +493,8 @@ def main():
                     help="prompts of the wave in the timed CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-group", type=int, default=4,
+                    help="prompts per copy/compute group of the host-memory e2e leg")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the ragged, 8K-prompt and decode timings")
     ap.add_argument("--prompts", type=int, default=32,

@@ -272,6 +272,53 @@ gdn_status gdn_prefill_packed_noalloc(const gdn_config* cfg, int32_t num_seqs,
                                       void* o, float* ckpt_states, float* final_states,
                                       void* stream);
 
+/* ---- prefill from host memory ---------------------------------------------------------- */
+
+/* The arrays of one pack, in the layouts of gdn_prefill_packed: inputs q, k, v, a, beta and
+ * initial_state (NULL = zeros), outputs o, ckpt_states (NULL when the pack has no
+ * checkpoints) and final_states. */
+typedef struct {
+  void* q;
+  void* k;
+  void* v;
+  float* a;
+  float* beta;
+  float* initial_state;
+  void* o;
+  float* ckpt_states;
+  float* final_states;
+} gdn_prefill_buffers;
+
+/* gdn_prefill_packed for a pack whose inputs and outputs live in host memory. The prompts
+ * are processed in groups of `group_prompts`. A group's rows of q, k, v, a, beta and its
+ * initial states are copied into `device` on the handle's copy-in stream; its prefill runs
+ * on `stream` (exactly as gdn_prefill_packed over that group); its o rows, checkpoints and
+ * final states are copied back into `host` on the handle's copy-out stream. The copies of
+ * neighbouring groups therefore overlap each other and the prefill: about the larger of
+ * the two copy volumes over the link rather than their sum. `stream` waits for the last
+ * copy out before anything queued after the call. Host buffers should be pinned
+ * (cudaHostAlloc) for full copy speed; `device` buffers are the pack-sized device arrays
+ * gdn_prefill_packed would take (their inputs are overwritten with the host inputs).
+ * Validation is that of gdn_prefill_packed on the whole pack and on `device`. Errors: also
+ * INVALID_ARGUMENT for a missing host array or group_prompts < 1, UNSUPPORTED for more than
+ * 64 groups. Results equal gdn_prefill_packed's on each group's sub-pack (the kernel
+ * schedule is chosen per group, so with the automatic choice they may differ from a
+ * whole-pack call by rounding). The workspace holds every group's work list, uploaded in
+ * one copy ahead of the bulk copies (gdn_prefill_host_workspace_size). */
+/* Device workspace bytes that gdn_prefill_packed_host needs for this pack and group size
+ * (the work lists of all groups). A multiple of 256. */
+gdn_status gdn_prefill_host_workspace_size(const gdn_config* cfg, int32_t num_seqs,
+                                           const int32_t* cu_seqlens_host,
+                                           const int32_t* ckpt_cu_host, int32_t group_prompts,
+                                           size_t* bytes);
+
+gdn_status gdn_prefill_packed_host(gdn_handle* handle, const gdn_config* cfg,
+                                   int32_t num_seqs, const int32_t* cu_seqlens_host,
+                                   const int32_t* ckpt_cu_host, const int32_t* ckpt_pos_host,
+                                   const gdn_prefill_buffers* host,
+                                   const gdn_prefill_buffers* device, int32_t group_prompts,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- sequence splitting ------------------------------------------------------------ */
 
 /* Device workspace bytes that gdn_prefill_packed_split needs for this pack and segment

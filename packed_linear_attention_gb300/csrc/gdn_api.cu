@@ -24,6 +24,7 @@ using gdn::GdnUnit;
 namespace {
 
 constexpr int kStagingSlots = 4;
+constexpr int kMaxHostGroups = 64;  // prompt groups of one gdn_prefill_packed_host call
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -53,6 +54,11 @@ struct gdn_handle {
   cudaEvent_t prefill_ready = nullptr;  // caller stream -> prefill stream
   cudaEvent_t prefill_done = nullptr;
   bool prefill_inflight = false;
+  // host-resident prefill: copy-in and copy-out streams, one event pair per prompt group
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t host_start = nullptr, host_done = nullptr;
+  cudaEvent_t group_in[kMaxHostGroups] = {};
+  cudaEvent_t group_out[kMaxHostGroups] = {};
 };
 
 namespace {
@@ -179,7 +185,7 @@ void build_worklist(void* dst, const ListLayout& L, KernelFamily fam, const gdn_
       for (int32_t r = 0; r < per_head; ++r) units[u++] = GdnUnit{n, h, r * rows, rows};
 }
 
-gdn_status plan(gdn_handle* h, const gdn_config* c, int32_t num_seqs, const int32_t* cu,
+gdn_status plan(const gdn_handle* h, const gdn_config* c, int32_t num_seqs, const int32_t* cu,
                 const int32_t* ckpt_cu, const int32_t* ckpt_pos, KernelFamily* fam,
                 ListLayout* L, int32_t* num_ckpt) {
   gdn_status s = check_config(c);
@@ -250,7 +256,14 @@ gdn_status gdn_handle_create(int32_t device, size_t pinned_pool_bytes, gdn_handl
             cudaEventCreateWithFlags(&h->compute_ready, cudaEventDisableTiming) == cudaSuccess &&
             cudaEventCreateWithFlags(&h->copy_done, cudaEventDisableTiming) == cudaSuccess &&
             cudaEventCreateWithFlags(&h->prefill_ready, cudaEventDisableTiming) == cudaSuccess &&
-            cudaEventCreateWithFlags(&h->prefill_done, cudaEventDisableTiming) == cudaSuccess;
+            cudaEventCreateWithFlags(&h->prefill_done, cudaEventDisableTiming) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&h->h2d, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&h->d2h, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h->host_start, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h->host_done, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; ok && i < kMaxHostGroups; ++i)
+    ok = cudaEventCreateWithFlags(&h->group_in[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&h->group_out[i], cudaEventDisableTiming) == cudaSuccess;
   for (int i = 0; ok && i < kStagingSlots; ++i)
     ok = cudaEventCreateWithFlags(&h->slots[i].done, cudaEventDisableTiming) == cudaSuccess;
   if (ok && pinned_pool_bytes > 0) {
@@ -275,6 +288,16 @@ gdn_status gdn_handle_destroy(gdn_handle* h) {
   if (h->prefill_stream && cudaStreamSynchronize(h->prefill_stream) != cudaSuccess)
     st = GDN_ERR_CUDA;
   if (h->side && cudaStreamSynchronize(h->side) != cudaSuccess) st = GDN_ERR_CUDA;
+  for (cudaStream_t s : {h->h2d, h->d2h})
+    if (s && cudaStreamSynchronize(s) != cudaSuccess) st = GDN_ERR_CUDA;
+  for (int i = 0; i < kMaxHostGroups; ++i) {
+    if (h->group_in[i]) cudaEventDestroy(h->group_in[i]);
+    if (h->group_out[i]) cudaEventDestroy(h->group_out[i]);
+  }
+  for (cudaEvent_t e : {h->host_start, h->host_done})
+    if (e) cudaEventDestroy(e);
+  for (cudaStream_t s : {h->h2d, h->d2h})
+    if (s) cudaStreamDestroy(s);
   for (int i = 0; i < kStagingSlots; ++i) {
     StagingSlot& s = h->slots[i];
     if (s.used && s.done) cudaEventSynchronize(s.done);
@@ -455,6 +478,193 @@ gdn_status gdn_prefill_packed(gdn_handle* h, const gdn_config* cfg, int32_t num_
   }
   if (prev != h->device) cudaSetDevice(prev);
   return s;
+}
+
+// ---- prefill from host memory --------------------------------------------------------------
+
+namespace {
+
+// One prompt group of gdn_prefill_packed_host: prompts [n0, n1), its sub-pack offsets and
+// the place of its work list in the workspace.
+struct HostGroup {
+  int32_t n0, n1, c0, c1;
+  std::vector<int32_t> cu, ck;
+  KernelFamily fam;
+  ListLayout L;
+  size_t off;
+};
+
+// Splits the pack into groups and lays their work lists out one after another. With
+// `sizing_only` the lists are sized for the family with the most units and the checkpoint
+// positions are not looked at.
+gdn_status plan_groups(const gdn_handle* h, const gdn_config* cfg, int32_t num_seqs,
+                       const int32_t* cu, const int32_t* ckpt_cu, const int32_t* ckpt_pos,
+                       int32_t group_prompts, bool sizing_only, std::vector<HostGroup>* out,
+                       size_t* total) {
+  if (group_prompts < 1) return GDN_ERR_INVALID_ARGUMENT;
+  gdn_status s = check_config(cfg);
+  if (s != GDN_OK) return s;
+  if (num_seqs < 1 || !cu || cu[0] != 0) return GDN_ERR_INVALID_ARGUMENT;
+  for (int32_t n = 0; n < num_seqs; ++n)
+    if (cu[n + 1] < cu[n]) return GDN_ERR_INVALID_ARGUMENT;
+  const int32_t groups = (num_seqs + group_prompts - 1) / group_prompts;
+  if (groups > kMaxHostGroups) return GDN_ERR_UNSUPPORTED;
+  out->clear();
+  *total = 0;
+  for (int32_t g = 0; g < groups; ++g) {
+    HostGroup G;
+    G.n0 = g * group_prompts;
+    G.n1 = std::min(num_seqs, G.n0 + group_prompts);
+    G.c0 = ckpt_cu ? ckpt_cu[G.n0] : 0;
+    G.c1 = ckpt_cu ? ckpt_cu[G.n1] : 0;
+    if (G.c1 < G.c0) return GDN_ERR_INVALID_ARGUMENT;
+    for (int32_t n = G.n0; n <= G.n1; ++n) G.cu.push_back(cu[n] - cu[G.n0]);
+    if (ckpt_cu)
+      for (int32_t n = G.n0; n <= G.n1; ++n) G.ck.push_back(ckpt_cu[n] - G.c0);
+    const int32_t ng = G.n1 - G.n0;
+    if (sizing_only) {
+      G.fam = kRecurrent;
+      const int64_t units = (int64_t)ng * cfg->num_v_heads * units_per_head(kRecurrent,
+                                                                            cfg->head_dim_v);
+      if (units > INT32_MAX) return GDN_ERR_UNSUPPORTED;
+      G.L = layout_for(ng, (int32_t)units, G.c1 - G.c0);
+    } else {
+      int32_t nck = 0;
+      s = plan(h, cfg, ng, G.cu.data(), ckpt_cu ? G.ck.data() : nullptr,
+               ckpt_pos ? ckpt_pos + G.c0 : nullptr, &G.fam, &G.L, &nck);
+      if (s != GDN_OK) return s;
+    }
+    G.off = *total;
+    *total += G.L.total;
+    out->push_back(std::move(G));
+  }
+  return GDN_OK;
+}
+
+}  // namespace
+
+gdn_status gdn_prefill_host_workspace_size(const gdn_config* cfg, int32_t num_seqs,
+                                           const int32_t* cu_seqlens_host,
+                                           const int32_t* ckpt_cu_host, int32_t group_prompts,
+                                           size_t* bytes) {
+  if (!bytes) return GDN_ERR_INVALID_ARGUMENT;
+  std::vector<HostGroup> groups;
+  size_t total = 0;
+  const gdn_status s = plan_groups(nullptr, cfg, num_seqs, cu_seqlens_host, ckpt_cu_host,
+                                   nullptr, group_prompts, true, &groups, &total);
+  if (s != GDN_OK) return s;
+  *bytes = total;
+  return GDN_OK;
+}
+
+gdn_status gdn_prefill_packed_host(gdn_handle* h, const gdn_config* cfg, int32_t num_seqs,
+                                   const int32_t* cu, const int32_t* ckpt_cu,
+                                   const int32_t* ckpt_pos, const gdn_prefill_buffers* host,
+                                   const gdn_prefill_buffers* dev, int32_t group_prompts,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  if (!h || !host || !dev) return GDN_ERR_INVALID_ARGUMENT;
+  // the whole pack is validated up front, as one gdn_prefill_packed call would be
+  KernelFamily fam;
+  ListLayout L;
+  int32_t num_ckpt = 0;
+  gdn_status s = plan(h, cfg, num_seqs, cu, ckpt_cu, ckpt_pos, &fam, &L, &num_ckpt);
+  if (s != GDN_OK) return s;
+  std::vector<HostGroup> groups;
+  size_t lists = 0;
+  s = plan_groups(h, cfg, num_seqs, cu, ckpt_cu, ckpt_pos, group_prompts, false, &groups,
+                  &lists);
+  if (s != GDN_OK) return s;
+  const int64_t T = cu[num_seqs];
+  s = check_buffers(cfg, num_seqs, T, num_ckpt, dev->q, dev->k, dev->v, dev->a, dev->beta,
+                    dev->initial_state, dev->o, dev->ckpt_states, dev->final_states, workspace,
+                    workspace_bytes, lists);
+  if (s != GDN_OK) return s;
+  if (T > 0 && (!host->q || !host->k || !host->v || !host->a || !host->beta || !host->o))
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (!host->final_states || (num_ckpt > 0 && !host->ckpt_states)) return GDN_ERR_INVALID_ARGUMENT;
+  if (!host->initial_state != !dev->initial_state) return GDN_ERR_INVALID_ARGUMENT;
+
+  const size_t es = cfg->io_dtype == GDN_BF16 ? 2 : 4;
+  const int D = cfg->head_dim_k;
+  const size_t qrow = (size_t)cfg->num_k_heads * D * es, vrow = (size_t)cfg->num_v_heads * D * es;
+  const size_t grow = (size_t)cfg->num_v_heads * 4, sb = (size_t)cfg->num_v_heads * D * D * 4;
+  auto at = [](const void* p, size_t off) {
+    return static_cast<char*>(const_cast<void*>(p)) + off;
+  };
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (prev != h->device && cudaSetDevice(h->device) != cudaSuccess) return GDN_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+
+  // every group's work list in one copy, queued ahead of the bulk copies
+  StagingSlot* slot = nullptr;
+  s = take_slot(h, lists, &slot);
+  cudaError_t e = cudaSuccess;
+  if (s == GDN_OK) {
+    char* img = static_cast<char*>(slot->host);
+    for (const HostGroup& G : groups)
+      build_worklist(img + G.off, G.L, G.fam, cfg, G.n1 - G.n0, G.cu.data(),
+                     ckpt_cu ? G.ck.data() : nullptr, ckpt_pos ? ckpt_pos + G.c0 : nullptr,
+                     G.c1 - G.c0);
+    e = cudaMemcpyAsync(ws, img, lists, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaEventRecord(slot->done, st);
+    slot->used = true;
+  }
+  // copies into the device buffers start after the work already queued on the caller's stream
+  if (s == GDN_OK && e == cudaSuccess) e = cudaEventRecord(h->host_start, st);
+  if (s == GDN_OK && e == cudaSuccess) e = cudaStreamWaitEvent(h->h2d, h->host_start, 0);
+  if (s == GDN_OK && e == cudaSuccess) e = cudaStreamWaitEvent(h->d2h, h->host_start, 0);
+  for (size_t g = 0; s == GDN_OK && e == cudaSuccess && g < groups.size(); ++g) {
+    const HostGroup& G = groups[g];
+    const size_t t0 = (size_t)cu[G.n0], nt = (size_t)(cu[G.n1] - cu[G.n0]);
+    // copy in: this group's token rows and initial states
+    auto in = [&](void* d, const void* hs, size_t off, size_t n) {
+      if (e == cudaSuccess && n > 0)
+        e = cudaMemcpyAsync(at(d, off), at(hs, off), n, cudaMemcpyHostToDevice, h->h2d);
+    };
+    in(dev->q, host->q, t0 * qrow, nt * qrow);
+    in(dev->k, host->k, t0 * qrow, nt * qrow);
+    in(dev->v, host->v, t0 * vrow, nt * vrow);
+    in(dev->a, host->a, t0 * grow, nt * grow);
+    in(dev->beta, host->beta, t0 * grow, nt * grow);
+    if (dev->initial_state)
+      in(dev->initial_state, host->initial_state, G.n0 * sb, (G.n1 - G.n0) * sb);
+    if (e == cudaSuccess) e = cudaEventRecord(h->group_in[g], h->h2d);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->group_in[g], 0);
+    if (e != cudaSuccess) break;
+    // the group's prefill: a sub-pack over the same buffers, rows and state slots offset
+    const gdn::PrefillArgs pa = prefill_args(
+        cfg, G.L, ws + G.off, reinterpret_cast<int32_t*>(ws), at(dev->q, t0 * qrow),
+        at(dev->k, t0 * qrow), at(dev->v, t0 * vrow),
+        reinterpret_cast<const float*>(at(dev->a, t0 * grow)),
+        reinterpret_cast<const float*>(at(dev->beta, t0 * grow)),
+        dev->initial_state ? reinterpret_cast<const float*>(at(dev->initial_state, G.n0 * sb))
+                           : nullptr,
+        at(dev->o, t0 * vrow),
+        G.c1 > G.c0 ? reinterpret_cast<float*>(at(dev->ckpt_states, G.c0 * sb)) : nullptr,
+        reinterpret_cast<float*>(at(dev->final_states, G.n0 * sb)));
+    if (launch_prefill(G.fam, h, cfg, pa, (int64_t)nt, stream) != 0) {
+      s = GDN_ERR_CUDA;
+      break;
+    }
+    // copy out once the group's prefill is done
+    e = cudaEventRecord(h->group_out[g], st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->d2h, h->group_out[g], 0);
+    auto out = [&](void* hd, const void* ds, size_t off, size_t n) {
+      if (e == cudaSuccess && n > 0)
+        e = cudaMemcpyAsync(at(hd, off), at(ds, off), n, cudaMemcpyDeviceToHost, h->d2h);
+    };
+    out(host->o, dev->o, t0 * vrow, nt * vrow);
+    if (G.c1 > G.c0) out(host->ckpt_states, dev->ckpt_states, G.c0 * sb, (G.c1 - G.c0) * sb);
+    out(host->final_states, dev->final_states, G.n0 * sb, (G.n1 - G.n0) * sb);
+  }
+  // the caller's stream completes after the last copy out
+  if (s == GDN_OK && e == cudaSuccess) e = cudaEventRecord(h->host_done, h->d2h);
+  if (s == GDN_OK && e == cudaSuccess) e = cudaStreamWaitEvent(st, h->host_done, 0);
+  if (prev != h->device) cudaSetDevice(prev);
+  if (s != GDN_OK) return s;
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 // ---- sequence splitting ------------------------------------------------------------------

@@ -44,7 +44,7 @@ EXPORTS = (
     "gdn_ckpt_position", "gdn_mixed_budget", "gdn_prefill_worklist_host",
     "gdn_prefill_packed_noalloc", "gdn_prefill_packed_async", "gdn_prefill_async_query",
     "gdn_prefill_async_wait", "gdn_prefill_async_join", "gdn_prefill_split_workspace_size",
-    "gdn_prefill_packed_split",
+    "gdn_prefill_packed_split", "gdn_prefill_packed_host", "gdn_prefill_host_workspace_size",
 )
 
 
@@ -52,6 +52,12 @@ class GdnError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class gdn_prefill_buffers(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_void_p) for name in
+                ("q", "k", "v", "a", "beta", "initial_state", "o", "ckpt_states",
+                 "final_states")]
 
 
 class gdn_config(ctypes.Structure):
@@ -94,6 +100,12 @@ def load(path: str = LIB_PATH):
                                                        ctypes.POINTER(ctypes.c_size_t)]),
             "gdn_prefill_packed_split": (I32, [P, CFG, I32, IP, P, P, P, P, P, P, IP, IP, P, P,
                                                P, I32, P, SZ, P]),
+            "gdn_prefill_host_workspace_size": (I32, [CFG, I32, IP, IP, I32,
+                                                      ctypes.POINTER(ctypes.c_size_t)]),
+            "gdn_prefill_packed_host": (I32, [P, CFG, I32, IP, IP, IP,
+                                              ctypes.POINTER(gdn_prefill_buffers),
+                                              ctypes.POINTER(gdn_prefill_buffers), I32, P, SZ,
+                                              P]),
             "gdn_read_device_status": (I32, [P, IP, P]),
             "gdn_prefill_packed_noalloc": (I32, [CFG, I32, IP, P, P, P, P, P, P, IP, IP, P, P,
                                                  P, P]),
@@ -235,6 +247,36 @@ def gdn_prefill_packed_split(handle, cfg, cu_seqlens, q, k, v, a, beta, initial_
         int(workspace_bytes), _stream(stream))
     if raise_on_error:
         _check(st, "gdn_prefill_packed_split")
+    return st
+
+
+def prefill_buffers(q, k, v, a, beta, initial_state, o, ckpt_states, final_states):
+    """A gdn_prefill_buffers record from tensors (or addresses, or None)."""
+    return gdn_prefill_buffers(*(_addr(x) for x in (q, k, v, a, beta, initial_state, o,
+                                                     ckpt_states, final_states)))
+
+
+def gdn_prefill_host_workspace_size(cfg: gdn_config, cu_seqlens, ckpt_cu=None,
+                                    group_prompts: int = 8) -> int:
+    n = ctypes.c_size_t()
+    _check(load().gdn_prefill_host_workspace_size(ctypes.byref(cfg), len(cu_seqlens) - 1,
+                                                  _i32(cu_seqlens), _i32(ckpt_cu),
+                                                  int(group_prompts), ctypes.byref(n)),
+           "gdn_prefill_host_workspace_size")
+    return n.value
+
+
+def gdn_prefill_packed_host(handle, cfg, cu_seqlens, ckpt_cu, ckpt_pos, host, device,
+                            group_prompts, workspace, workspace_bytes, stream=None, *,
+                            raise_on_error=True) -> int:
+    """gdn_prefill_packed for host-resident inputs and outputs, copies overlapped per group
+    of prompts. `host` and `device` are gdn_prefill_buffers records."""
+    st = load().gdn_prefill_packed_host(
+        handle, ctypes.byref(cfg), len(cu_seqlens) - 1, _i32(cu_seqlens), _i32(ckpt_cu),
+        _i32(ckpt_pos), ctypes.byref(host), ctypes.byref(device), int(group_prompts),
+        _addr(workspace), int(workspace_bytes), _stream(stream))
+    if raise_on_error:
+        _check(st, "gdn_prefill_packed_host")
     return st
 
 

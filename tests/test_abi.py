@@ -169,3 +169,20 @@ def test_gate_mode_validation(lib):
     bad.gate_mode = 2
     with pytest.raises(gdn.GdnError):
         gdn.gdn_prefill_workspace_size(bad, cu)
+
+
+def test_host_workspace_size(lib):
+    """gdn_prefill_packed_host's workspace holds one work list per prompt group: at least
+    the whole pack's, growing with the number of groups; bad group sizes are rejected."""
+    cfg = gdn.make_config(**CFG)
+    cu = list(range(0, 33 * 1024, 1024))
+    whole = gdn.gdn_prefill_workspace_size(cfg, cu)
+    sizes = [gdn.gdn_prefill_host_workspace_size(cfg, cu, group_prompts=g) for g in (32, 8, 1)]
+    assert all(x % 256 == 0 for x in sizes)
+    assert sizes[0] >= whole and sizes[0] <= sizes[1] <= sizes[2]
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.gdn_prefill_host_workspace_size(cfg, cu, group_prompts=0)
+    assert e.value.status == gdn.GDN_ERR_INVALID_ARGUMENT
+    with pytest.raises(gdn.GdnError) as e:  # more than 64 groups
+        gdn.gdn_prefill_host_workspace_size(cfg, list(range(0, 66 * 8, 8)), group_prompts=1)
+    assert e.value.status == gdn.GDN_ERR_UNSUPPORTED
