@@ -291,12 +291,13 @@ def run_gpu(args):
     ms_local = sum(per) / len(per)
     ms, value = aggregate(T, ms_local, world, dev)
 
-    # the chunked kernel's automatic schedule choice (same rule as the library's)
+    # the chunked kernel's automatic schedule choice (asked of the library)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    schedule = ("chunked, throughput schedule" if N * Hv >= 6 * sms
+    choice = gdn.gdn_chunked_schedule(pack.cu_seqlens, Hv, sms)
+    schedule = ("chunked, throughput schedule" if choice == gdn.KERNEL_CHUNKED_THROUGHPUT
                 else "chunked, pipelined schedule") + f" ({N * Hv} units on {sms} SMs)"
 
-    # roofline of the prefill kernel (the only kernel of the step)
+    # roofline of the step's prefill launches (the only kernels of the step)
     hbm_gbs, tflops, peak_src = load_peaks()
     B = algorithmic_bytes(T, Hk, Hv, d, N, pack.num_ckpts)
     F = algorithmic_flops(T, Hk, Hv, d)
@@ -389,13 +390,17 @@ def run_secondary(torch, gdn, I, h, stream, flush, hbm_gbs):
     the ragged prefix-cache pack, 4 x 8K prompts, and the one-token decode step of 32
     sequences (HBM-bound: every state byte read and written once)."""
     out = {}
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     for name, pack in (("ragged_prefix_8", I.ragged_prefix()), ("long_4x8192", I.long_prompts())):
         buf = gdn.to_device(pack)
         ms = _time_events(torch, lambda: gdn.prefill(h, buf, stream), stream, flush)
         B = algorithmic_bytes(pack.total_tokens, 16, 32, 128, pack.num_seqs, pack.num_ckpts,
                               init=pack.init is not None)
         out[name] = {"tokens": pack.total_tokens, "us": ms * 1e3,
-                     "schedule": "chunked, pipelined (automatic choice: few units per SM)",
+                     "schedule": "chunked, " + (
+                         "throughput" if gdn.gdn_chunked_schedule(pack.cu_seqlens, 32, sms)
+                         == gdn.KERNEL_CHUNKED_THROUGHPUT else "pipelined") +
+                     " schedule (automatic choice)",
                      "tokens_per_s": pack.total_tokens / (ms / 1e3),
                      "achieved_gbs": B / (ms / 1e3) / 1e9, "frac_hbm": B / (ms / 1e3) / 1e9 / hbm_gbs}
         del buf

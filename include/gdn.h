@@ -114,16 +114,30 @@ gdn_status gdn_pool_info(gdn_handle* handle, void** host_ptr, size_t* bytes);
 
 /* Kernel choice for later prefill calls on this handle:
  *   0 = automatic: the tensor-core chunked kernel where it applies (bf16 io, d = 128),
- *       in its throughput schedule (two CTAs per SM) when the pack has at least six
- *       (prompt, value head) units per SM, else in its pipelined schedule (one CTA per SM,
- *       the next chunk's state-independent work overlapped with the current recurrence);
- *       otherwise the token-serial CUDA-core kernel;
+ *       in the schedule gdn_chunked_schedule names for the pack; otherwise the
+ *       token-serial CUDA-core kernel;
  *   1 = always the token-serial kernel (a cross-check path);
  *   2 = the chunked kernel's pipelined schedule, 3 = its throughput schedule (where the
  *       chunked kernel applies; otherwise the token-serial kernel).
- * Every choice computes the same recurrence; results agree to rounding (each schedule is
- * deterministic and packing-independent on its own). Errors: INVALID_ARGUMENT. */
+ * The two chunked schedules give bit-identical results, so choices 0, 2 and 3 agree bit
+ * for bit, and a prompt's results do not depend on the pack around it even where the
+ * automatic choice differs; the token-serial kernel agrees with them to rounding. Errors: INVALID_ARGUMENT. */
 gdn_status gdn_set_kernel_preference(gdn_handle* handle, int32_t preference);
+
+/* The chunked kernel's schedule that the automatic choice takes for a pack of `num_seqs`
+ * prompts (cu_seqlens_host: prefix sums, as for gdn_prefill_packed) with `num_v_heads`
+ * value heads on a GPU with `num_sms` SMs: *schedule = 2 (pipelined) or 3 (throughput),
+ * the gdn_set_kernel_preference codes. The choice is the smaller of two estimates from
+ * per-chunk costs measured on GB300 (6.4 us per chunk for a pipelined unit on its own SM,
+ * 9.5 us for a throughput unit alone on its SM, 11.6 us for one of two sharing an SM), over
+ * W = the chunks of all (prompt, value head) units and Lmax = the chunks of the longest:
+ *   pipelined:  6.4 max(Lmax, W / num_sms)
+ *   throughput: max(9.5 Lmax, 11.6 W / (2 num_sms)).
+ * Both schedules give bit-identical results; only the time differs. Host-only arithmetic,
+ * no CUDA call. Errors: INVALID_ARGUMENT (num_seqs < 0, cu NULL with num_seqs > 0,
+ * cu[0] != 0 or decreasing, num_v_heads < 1, num_sms < 1, schedule NULL). */
+gdn_status gdn_chunked_schedule(int32_t num_seqs, const int32_t* cu_seqlens_host,
+                                int32_t num_v_heads, int32_t num_sms, int32_t* schedule);
 
 /* Device workspace bytes that gdn_prefill_packed needs for this pack (the chunk/tile work
  * list). Validates the same arguments gdn_prefill_packed validates about the pack.

@@ -329,6 +329,17 @@ gdn_status gdn_set_kernel_preference(gdn_handle* h, int32_t pref) {
   return GDN_OK;
 }
 
+gdn_status gdn_chunked_schedule(int32_t num_seqs, const int32_t* cu, int32_t num_v_heads,
+                                int32_t num_sms, int32_t* schedule) {
+  if (num_seqs < 0 || (num_seqs > 0 && !cu) || num_v_heads < 1 || num_sms < 1 || !schedule)
+    return GDN_ERR_INVALID_ARGUMENT;
+  for (int32_t n = 0; n < num_seqs; ++n)
+    if (cu[n + 1] < cu[n]) return GDN_ERR_INVALID_ARGUMENT;
+  if (num_seqs > 0 && cu[0] != 0) return GDN_ERR_INVALID_ARGUMENT;
+  *schedule = gdn::plan_schedule(gdn::chunk_load(cu, num_seqs, num_v_heads), num_sms);
+  return GDN_OK;
+}
+
 gdn_status gdn_prefill_workspace_size(const gdn_config* cfg, int32_t num_seqs,
                                       const int32_t* cu_seqlens_host,
                                       const int32_t* ckpt_cu_host, size_t* bytes) {
@@ -427,11 +438,13 @@ gdn::PrefillArgs prefill_args(const gdn_config* cfg, const ListLayout& L, char* 
   return pa;
 }
 
+// `load`: the pack's chunk counts, for the chunked kernel's automatic schedule choice.
 int launch_prefill(KernelFamily fam, const gdn_handle* h, const gdn_config* cfg,
-                   const gdn::PrefillArgs& pa, int64_t T, void* stream) {
+                   const gdn::PrefillArgs& pa, int64_t T, const gdn::ChunkLoad& load,
+                   void* stream) {
   if (fam == kChunked) {
     const int schedule = h && h->kernel_pref >= 2 ? h->kernel_pref : gdn::kChunkedAuto;
-    return gdn::launch_chunked_prefill(pa, T, schedule, stream);
+    return gdn::launch_chunked_prefill(pa, T, schedule, load, stream);
   }
   return gdn::launch_recurrent_prefill(pa, cfg->head_dim_k, cfg->io_dtype == GDN_BF16, stream);
 }
@@ -474,7 +487,9 @@ gdn_status gdn_prefill_packed(gdn_handle* h, const gdn_config* cfg, int32_t num_
     const gdn::PrefillArgs pa =
         prefill_args(cfg, L, ws, reinterpret_cast<int32_t*>(ws), q, k, v, a, beta, init, o,
                      ckpt_states, final_states);
-    if (launch_prefill(fam, h, cfg, pa, T, stream) != 0) s = GDN_ERR_CUDA;
+    if (launch_prefill(fam, h, cfg, pa, T, gdn::chunk_load(cu, num_seqs, cfg->num_v_heads),
+                       stream) != 0)
+      s = GDN_ERR_CUDA;
   }
   if (prev != h->device) cudaSetDevice(prev);
   return s;
@@ -644,7 +659,9 @@ gdn_status gdn_prefill_packed_host(gdn_handle* h, const gdn_config* cfg, int32_t
         at(dev->o, t0 * vrow),
         G.c1 > G.c0 ? reinterpret_cast<float*>(at(dev->ckpt_states, G.c0 * sb)) : nullptr,
         reinterpret_cast<float*>(at(dev->final_states, G.n0 * sb)));
-    if (launch_prefill(G.fam, h, cfg, pa, (int64_t)nt, stream) != 0) {
+    if (launch_prefill(G.fam, h, cfg, pa, (int64_t)nt,
+                       gdn::chunk_load(cu + G.n0, G.n1 - G.n0, cfg->num_v_heads),
+                       stream) != 0) {
       s = GDN_ERR_CUDA;
       break;
     }
@@ -674,6 +691,16 @@ namespace {
 struct VSeq {
   int32_t tok_start, len, ckpt_begin, ckpt_end, flags;
 };
+
+gdn::ChunkLoad vseq_load(const std::vector<VSeq>& vs, int32_t units_per_prompt) {
+  gdn::ChunkLoad l;
+  for (const VSeq& x : vs) {
+    const int32_t c = (x.len + 63) / 64;
+    l.total += (int64_t)c * units_per_prompt;
+    l.longest = std::max(l.longest, c);
+  }
+  return l;
+}
 
 // Work-list image for a list of virtual prompts (same layout and longest-first order as
 // build_worklist); ckpt positions are copied as given.
@@ -874,7 +901,7 @@ gdn_status gdn_prefill_packed_split(gdn_handle* h, const gdn_config* cfg, int32_
       e = launch_prefill(fam, h, cfg,
                          prefill_args(cfg, P.la, ws, status, q, k, v, a, beta, init_a, o,
                                       ckpt_states, fin_a),
-                         T, stream);
+                         T, vseq_load(P.va, hv), stream);
     // the initial states of segments 1 .. P-1, then pass C
     if (e == 0)
       e = gdn::launch_compose_maps(reinterpret_cast<const gdn::SplitCompose*>(ws + P.off_jobs),
@@ -883,7 +910,7 @@ gdn_status gdn_prefill_packed_split(gdn_handle* h, const gdn_config* cfg, int32_
       e = launch_prefill(fam, h, cfg,
                          prefill_args(cfg, P.lc, ws + P.off_c, status, q, k, v, a, beta, init_c,
                                       o, ckpt_states, fin_c),
-                         T, stream);
+                         T, vseq_load(P.vc, hv), stream);
     if (e == 0)
       e = gdn::launch_gather_states(final_states, fin_a, fin_c,
                                     reinterpret_cast<const int32_t*>(ws + P.off_gather),

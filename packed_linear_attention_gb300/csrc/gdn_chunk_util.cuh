@@ -1,7 +1,8 @@
 // gdn_chunk_util.cuh — device helpers shared by the two schedules of the chunked prefill
 // kernel (gdn_chunked.cu, gdn_chunked_pipe.cu): fp16 packing into 128B-swizzled operand
-// tiles, the bf16 -> fp16 widening of q/k/v, the gate loads of a chunk and the warp-level
-// tf32 tile products of the 64 x 64 triangular inverse.
+// tiles, the bf16 -> fp16 widening of q/k/v, the gate loads of a chunk, the per-token gate
+// factors (one code path, so that both schedules compute them bit for bit alike) and the
+// warp-level tf32 tile products of the 64 x 64 triangular inverse.
 #pragma once
 #include <cuda_fp16.h>
 
@@ -90,6 +91,68 @@ __device__ __forceinline__ void gates_of(const float (&raw_g)[4], int t0, int le
     g[hh] = live ? a : 0.f;
     g[2 + hh] = live ? b : 0.f;
   }
+}
+
+// Per-token factors of one chunk: eight 64-float arrays from one base.
+struct Factors {
+  float* G;    // log2-scaled inclusive cumulative log-decay
+  float* B;    // beta
+  float* Gq;   // scale e^{G_t} / |q_t|: row factor of Q~
+  float* BG;   // beta_j e^{G_j} / |k_j|: column factor of T1
+  float* Dec;  // e^{G_L - G_j} / |k_j|: row factor of D'
+  float* Gp;   // G_j - log2(1/|k_j|): column exponent of A and P
+  float* Rk;   // 1/|k_j|
+  float* Rq;   // 1/|q_t|
+  __device__ explicit Factors(float* base)
+      : G(base), B(base + 64), Gq(base + 128), BG(base + 192), Dec(base + 256),
+        Gp(base + 320), Rk(base + 384), Rq(base + 448) {}
+};
+
+// Chunk-local inclusive cumulative log-decay (log2 units) of tokens lane and lane + 32 by
+// a warp scan (a0, a1); returns the chunk total G_L. Every product and sum is rounded on
+// its own (no contraction), so that every caller, in either schedule, gets the same bits.
+__device__ __forceinline__ float gate_scan(const float (&g)[4], int lane, float& a0,
+                                           float& a1) {
+  a0 = __fmul_rn(g[0], kLog2e);
+  a1 = __fmul_rn(g[1], kLog2e);
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y0 = __shfl_up_sync(0xffffffffu, a0, off);
+    const float y1 = __shfl_up_sync(0xffffffffu, a1, off);
+    if (lane >= off) {
+      a0 = __fadd_rn(a0, y0);
+      a1 = __fadd_rn(a1, y1);
+    }
+  }
+  a1 = __fadd_rn(a1, __shfl_sync(0xffffffffu, a0, 31));
+  return __shfl_sync(0xffffffffu, a1, 31);  // padded tokens add nothing
+}
+
+// e^{G_L} of a chunk from its gates (one warp): the state's decay over the chunk.
+__device__ __forceinline__ float chunk_decay(const float (&g)[4], int lane) {
+  float a0, a1;
+  return ptx::ex2(gate_scan(g, lane, a0, a1));
+}
+
+// The gate factors of one chunk from its gates (one warp, tokens lane and lane + 32); the
+// norms are folded in later. Returns e^{G_L}.
+__device__ __forceinline__ float write_gate_factors(const Factors& f, const float (&g)[4],
+                                                    float scale, int lane) {
+  float a0, a1;
+  const float gl = gate_scan(g, lane, a0, a1);
+  const float b0 = g[2], b1 = g[3];
+  const float e0 = ptx::ex2(a0), e1 = ptx::ex2(a1);
+  f.G[lane] = a0;
+  f.G[lane + 32] = a1;
+  f.B[lane] = b0;
+  f.B[lane + 32] = b1;
+  f.Gq[lane] = __fmul_rn(scale, e0);
+  f.Gq[lane + 32] = __fmul_rn(scale, e1);
+  f.BG[lane] = __fmul_rn(b0, e0);
+  f.BG[lane + 32] = __fmul_rn(b1, e1);
+  f.Dec[lane] = ptx::ex2(__fsub_rn(gl, a0));
+  f.Dec[lane + 32] = ptx::ex2(__fsub_rn(gl, a1));
+  return ptx::ex2(gl);
 }
 
 // One 16 x 8 output tile D = sum_k Ablk[r0.., k] * Bblk[k.., n0..] over k in [k_lo, k_hi)

@@ -256,10 +256,8 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
   const float dt_bias = raw ? __ldg(p.dt_bias + h) : 0.f;
   if (warp == 0 && nchunks > 0) {
     load_gates(ag, bg, p.hv_heads, 0, sd.len, lane, raw, a_log, dt_bias, gnext);
-    float s = gnext[0] + gnext[1];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) sm.next_decay = __expf(s);
+    const float d = chunk_decay(gnext, lane);
+    if (lane == 0) sm.next_decay = d;
   }
   tc_fence_before();
   __syncthreads();
@@ -304,27 +302,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
 
     // ---- (1) gates of this chunk from registers; fetch the next chunk's ------------------
     if (warp == 0) {
-      float a0 = gnext[0] * kLog2e, a1 = gnext[1] * kLog2e;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float y0 = __shfl_up_sync(0xffffffffu, a0, off);
-        const float y1 = __shfl_up_sync(0xffffffffu, a1, off);
-        if (lane >= off) { a0 += y0; a1 += y1; }
-      }
-      a1 += __shfl_sync(0xffffffffu, a0, 31);
-      const float gl = __shfl_sync(0xffffffffu, a1, 31);  // padded tokens add nothing
-      const float b0 = gnext[2], b1 = gnext[3];
-      const float e0 = ex2(a0), e1 = ex2(a1);
-      sG[lane] = a0;
-      sG[lane + 32] = a1;
-      sB[lane] = b0;
-      sB[lane + 32] = b1;
-      sGq[lane] = scale * e0;
-      sGq[lane + 32] = scale * e1;
-      sBG[lane] = b0 * e0;
-      sBG[lane + 32] = b1 * e1;
-      sDec[lane] = ex2(gl - a0);
-      sDec[lane + 32] = ex2(gl - a1);
+      write_gate_factors(Factors(sG), gnext, scale, lane);
       if (c + 1 < nchunks)
         load_gates(ag, bg, p.hv_heads, t0 + kC, sd.len, lane, raw, a_log, dt_bias, gnext);
     }
@@ -595,10 +573,8 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       }
       // total decay of the next chunk, for the state pre-scale after this chunk
       if (warp == 0 && c + 1 < nchunks) {
-        float s = gnext[0] + gnext[1];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (lane == 0) sm.next_decay = __expf(s);
+        const float d = chunk_decay(gnext, lane);
+        if (lane == 0) sm.next_decay = d;
       }
     }
     publish_operands();

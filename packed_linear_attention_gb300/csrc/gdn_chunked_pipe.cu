@@ -258,21 +258,6 @@ __device__ void invert_merge(const float* A, float* T, float* X, uint8_t* T1, ui
   named_sync(kBarPrep, kGroup);
 }
 
-// Per-token factors of one chunk (one buffer of 8 x 64 floats).
-struct Factors {
-  float* G;    // log2-scaled inclusive cumulative log-decay
-  float* B;    // beta
-  float* Gq;   // scale e^{G_t} / |q_t|: row factor of Q~
-  float* BG;   // beta_j e^{G_j} / |k_j|: column factor of T1
-  float* Dec;  // e^{G_L - G_j} / |k_j|: row factor of D'
-  float* Gp;   // G_j - log2(1/|k_j|): column exponent of A and P
-  float* Rk;   // 1/|k_j|
-  float* Rq;   // 1/|q_t|
-  __device__ explicit Factors(float* base)
-      : G(base), B(base + 64), Gq(base + 128), BG(base + 192), Dec(base + 256),
-        Gp(base + 320), Rk(base + 384), Rq(base + 448) {}
-};
-
 // q and k of one chunk to fp16 in place (exact: bf16 values are fp16 values) with their
 // inverse L2 norms into f.Rk / f.Rq; rows past the chunk's L tokens are zeroed. The norms
 // are not applied to the tiles: they are folded into per-token factors. One warp group
@@ -336,35 +321,6 @@ __device__ __forceinline__ void convert_v(uint8_t* sV, int L, int gtid) {
     *reinterpret_cast<uint4*>(sV + reg * 8192 + (r >> 3) * 1024 + (r & 7) * 128 +
                               ((cc ^ (r & 7)) << 4)) = (int)r < L ? bf16x8_to_half8(w[pass]) : zero;
   }
-}
-
-// The gate factors of one chunk from its gates (one warp, tokens lane and lane + 32):
-// chunk-local inclusive cumulative log-decay (log2 units) by a warp scan, and the factors
-// built from it. The norms are folded in later by the prep group. Returns e^{G_L}.
-__device__ __forceinline__ float write_gate_factors(const Factors& f, const float (&g)[4],
-                                                    float scale, int lane) {
-  float a0 = g[0] * kLog2e, a1 = g[1] * kLog2e;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const float y0 = __shfl_up_sync(0xffffffffu, a0, off);
-    const float y1 = __shfl_up_sync(0xffffffffu, a1, off);
-    if (lane >= off) { a0 += y0; a1 += y1; }
-  }
-  a1 += __shfl_sync(0xffffffffu, a0, 31);
-  const float gl = __shfl_sync(0xffffffffu, a1, 31);  // padded tokens add nothing
-  const float b0 = g[2], b1 = g[3];
-  const float e0 = ex2(a0), e1 = ex2(a1);
-  f.G[lane] = a0;
-  f.G[lane + 32] = a1;
-  f.B[lane] = b0;
-  f.B[lane + 32] = b1;
-  f.Gq[lane] = scale * e0;
-  f.Gq[lane + 32] = scale * e1;
-  f.BG[lane] = b0 * e0;
-  f.BG[lane + 32] = b1 * e1;
-  f.Dec[lane] = ex2(gl - a0);
-  f.Dec[lane + 32] = ex2(gl - a1);
-  return ex2(gl);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)

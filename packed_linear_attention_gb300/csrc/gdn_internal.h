@@ -106,14 +106,31 @@ int launch_decode(const DecodeArgs& a, int head_dim, bool bf16, void* stream);
 //  * pipelined (gdn_chunked_pipe.cu): one 16-warp CTA per SM whose two warp groups overlap
 //    the state-independent work of the next chunk with the recurrence of the current one;
 //    shortest time per unit, so best for packs with few units per SM or very long prompts.
-// kChunkedAuto takes the throughput schedule when the pack has at least
-// kThroughputUnitsPerSM units per SM.
+// kChunkedAuto takes the one with the smaller estimated time (plan_schedule).
 enum ChunkedSchedule : int { kChunkedAuto = 0, kChunkedPipelined = 2, kChunkedThroughput = 3 };
-constexpr int kThroughputUnitsPerSM = 6;
+constexpr int kThroughputCtasPerSM = 2;  // resident throughput CTAs per SM
+
+// Chunk counts of a pack's work list: over all units, and of the longest unit.
+struct ChunkLoad {
+  int64_t total = 0;
+  int32_t longest = 0;
+};
+// The load of a pack of prompts (cu: host prefix sums) with `units_per_prompt` units each.
+inline ChunkLoad chunk_load(const int32_t* cu, int32_t num_seqs, int32_t units_per_prompt) {
+  ChunkLoad l;
+  for (int32_t n = 0; n < num_seqs; ++n) {
+    const int32_t c = (cu[n + 1] - cu[n] + 63) / 64;
+    l.total += (int64_t)c * units_per_prompt;
+    if (c > l.longest) l.longest = c;
+  }
+  return l;
+}
+// kChunkedPipelined or kChunkedThroughput for a pack of this load on `num_sms` SMs.
+int plan_schedule(const ChunkLoad& load, int32_t num_sms);
 int launch_chunked_throughput(const PrefillArgs& a, int64_t total_tokens, void* stream);
 int launch_chunked_pipelined(const PrefillArgs& a, int64_t total_tokens, void* stream);
 int launch_chunked_prefill(const PrefillArgs& a, int64_t total_tokens, int schedule,
-                           void* stream);
+                           const ChunkLoad& load, void* stream);
 
 // 2D bf16 tensor maps (64 x 64 boxes, 128-byte swizzle, zero fill past the last row) over
 // q, k (H_k * d columns) and v (H_v * d columns) with total_tokens rows (gdn_tma.cu).

@@ -122,7 +122,9 @@ extern "C" gdn_status gdn_prefill_packed_noalloc(const gdn_config* cfg, int32_t 
   pa.a_log = cfg->a_log;
   pa.dt_bias = cfg->dt_bias;
   const int e = plan.family == 2
-                    ? gdn::launch_chunked_prefill(pa, T, gdn::kChunkedAuto, stream)
+                    ? gdn::launch_chunked_prefill(pa, T, gdn::kChunkedAuto,
+                                                  gdn::chunk_load(cu, num_seqs, cfg->num_v_heads),
+                                                  stream)
                     : gdn::launch_recurrent_prefill(pa, D, cfg->io_dtype == GDN_BF16, stream);
   return e == 0 ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -62,8 +63,21 @@ bool make_qkv_maps(const PrefillArgs& a, int64_t total_tokens, int head_dim, CUt
          make_bf16_map(tv, a.v, (uint64_t)a.hv_heads * head_dim, rows);
 }
 
+// Estimated times from per-chunk costs measured on GB300 with 1,024-token units (tenths of
+// a microsecond per chunk): a pipelined unit on its own SM, a throughput CTA alone on its
+// SM, and a throughput CTA sharing its SM with a second one. A pack takes at least its
+// longest unit's chain and at least its total work spread over the SMs' slots.
+int plan_schedule(const ChunkLoad& load, int32_t num_sms) {
+  constexpr double kPipe = 64, kThroughputAlone = 95, kThroughputPaired = 116;
+  const double longest = load.longest, total = (double)load.total, sms = num_sms;
+  const double t_pipe = kPipe * std::max(longest, total / sms);
+  const double t_thr = std::max(kThroughputAlone * longest,
+                                kThroughputPaired * total / (kThroughputCtasPerSM * sms));
+  return t_thr < t_pipe ? kChunkedThroughput : kChunkedPipelined;
+}
+
 int launch_chunked_prefill(const PrefillArgs& a, int64_t total_tokens, int schedule,
-                           void* stream) {
+                           const ChunkLoad& load, void* stream) {
   if (schedule == kChunkedAuto) {
     static int sms[64] = {0};  // SM count per device, asked once
     int dev = 0;
@@ -75,8 +89,7 @@ int launch_chunked_prefill(const PrefillArgs& a, int64_t total_tokens, int sched
       if (e != cudaSuccess) return (int)e;
       if (dev >= 0 && dev < 64) sms[dev] = n;
     }
-    schedule = (int64_t)a.num_units >= (int64_t)kThroughputUnitsPerSM * n ? kChunkedThroughput
-                                                                          : kChunkedPipelined;
+    schedule = plan_schedule(load, n);
   }
   return schedule == kChunkedThroughput ? launch_chunked_throughput(a, total_tokens, stream)
                                         : launch_chunked_pipelined(a, total_tokens, stream);

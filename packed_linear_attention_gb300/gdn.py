@@ -45,6 +45,7 @@ EXPORTS = (
     "gdn_prefill_packed_noalloc", "gdn_prefill_packed_async", "gdn_prefill_async_query",
     "gdn_prefill_async_wait", "gdn_prefill_async_join", "gdn_prefill_split_workspace_size",
     "gdn_prefill_packed_split", "gdn_prefill_packed_host", "gdn_prefill_host_workspace_size",
+    "gdn_chunked_schedule",
 )
 
 
@@ -93,6 +94,7 @@ def load(path: str = LIB_PATH):
             "gdn_handle_destroy": (I32, [P]),
             "gdn_pool_info": (I32, [P, ctypes.POINTER(P), ctypes.POINTER(SZ)]),
             "gdn_set_kernel_preference": (I32, [P, I32]),
+            "gdn_chunked_schedule": (I32, [I32, IP, I32, I32, IP]),
             "gdn_prefill_workspace_size": (I32, [CFG, I32, IP, IP, ctypes.POINTER(SZ)]),
             "gdn_prefill_packed": (I32, [P, CFG, I32, IP, P, P, P, P, P, P, IP, IP, P, P, P,
                                          P, SZ, P]),
@@ -200,6 +202,15 @@ def gdn_pool_info(handle: int) -> tuple[int, int]:
 def gdn_set_kernel_preference(handle: int, preference: int) -> None:
     _check(load().gdn_set_kernel_preference(handle, int(preference)),
            "gdn_set_kernel_preference")
+
+
+def gdn_chunked_schedule(cu_seqlens, num_v_heads: int, num_sms: int) -> int:
+    """The chunked schedule the automatic choice takes for this pack: KERNEL_CHUNKED_PIPELINED
+    or KERNEL_CHUNKED_THROUGHPUT."""
+    out = ctypes.c_int32()
+    _check(load().gdn_chunked_schedule(len(cu_seqlens) - 1, _i32(cu_seqlens), int(num_v_heads),
+                                       int(num_sms), ctypes.byref(out)), "gdn_chunked_schedule")
+    return out.value
 
 
 def gdn_prefill_workspace_size(cfg: gdn_config, cu_seqlens, ckpt_cu=None) -> int:

@@ -186,3 +186,35 @@ def test_host_workspace_size(lib):
     with pytest.raises(gdn.GdnError) as e:  # more than 64 groups
         gdn.gdn_prefill_host_workspace_size(cfg, list(range(0, 66 * 8, 8)), group_prompts=1)
     assert e.value.status == gdn.GDN_ERR_UNSUPPORTED
+
+
+def test_chunked_schedule_choice(lib):
+    """The automatic choice between the chunked kernel's schedules against the cost model
+    written out here, on the packs whose times were measured: pipelined for one unit per
+    SM, for the ragged prefix-cache pack and for 8K prompts; throughput for two or more
+    units per SM of 1,024-token prompts and for the 32 x 1,024 wave."""
+    pipe, thr = gdn.KERNEL_CHUNKED_PIPELINED, gdn.KERNEL_CHUNKED_THROUGHPUT
+    choose = gdn.gdn_chunked_schedule
+    cu = lambda lens: np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    assert choose(cu([1024] * 19), 8, 152) == pipe      # 152 units: one per SM
+    assert choose(cu([1024] * 38), 8, 152) == thr       # 304 units
+    assert choose(cu([1024] * 76), 8, 152) == thr       # 608 units
+    assert choose(cu([1024] * 32), 32, 152) == thr      # the wave
+    r = I.ragged_prefix()
+    assert choose(r.cu_seqlens, 32, 152) == pipe
+    assert choose(cu([8192] * 4), 32, 152) == pipe
+    assert choose(cu([]), 32, 152) == pipe              # empty pack
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        lens = rng.integers(0, 5000, rng.integers(1, 40))
+        hv, sms = int(rng.choice([4, 8, 32, 64])), int(rng.choice([1, 132, 152]))
+        ch = (lens + 63) // 64
+        W, L = float(ch.sum() * hv), float(ch.max())
+        t_pipe = 64 * max(L, W / sms)
+        t_thr = max(95 * L, 116 * W / (2 * sms))
+        assert choose(cu(lens), hv, sms) == (thr if t_thr < t_pipe else pipe)
+    for bad in ((cu([3]), 0, 152), (cu([3]), 8, 0), (np.array([1, 4], np.int32), 8, 152),
+                (np.array([0, 4, 2], np.int32), 8, 152)):
+        with pytest.raises(gdn.GdnError) as e:
+            choose(*bad)
+        assert e.value.status == gdn.GDN_ERR_INVALID_ARGUMENT

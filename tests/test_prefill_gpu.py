@@ -206,16 +206,65 @@ def test_checkpoint_copy_to_pinned_pool(ragged):
         gdn.gdn_checkpoint_copy(h, buf.ckpt, size, 16, stream)
 
 
-def test_automatic_schedule_choice(wave):
-    """Automatic choice: the pipelined schedule for a pack with few units per SM, the
-    throughput schedule for the full wave (the schedules round differently, so a bitwise
-    match identifies the one that ran)."""
+def _assert_same(a, b):
+    for x, y, what in zip(a, b, ("o", "ckpt", "final")):
+        np.testing.assert_array_equal(x, y, err_msg=what)
+
+
+@pytest.mark.parametrize("case", ["edges_init", "raw_gates", "ragged", "long"])
+def test_chunked_schedules_agree_bitwise(case, ragged):
+    """The pipelined and throughput schedules compute every value the same way (same
+    operand roundings, same product accumulation order, the same gate scan), so their
+    outputs, checkpoints and final states are bit-identical."""
     torch_cuda()
-    small = I.make_pack([200, 64, 900], num_k_heads=16, num_v_heads=32, head_dim=128,
-                        io_dtype="bf16", seed=8, init_std=0.02)
-    auto = run(small)
-    for x, y in zip(auto, run(small, gdn.KERNEL_CHUNKED_PIPELINED)):
-        np.testing.assert_array_equal(x, y)
+    if case == "edges_init":
+        lengths = [1, 0, 63, 64, 65, 129, 200, 3, 1000]
+        ck = [[x for x in range(64, n + 1, 64)] + ([n] if n % 64 and n > 0 else [])
+              for n in lengths]
+        p = I.make_pack(lengths, num_k_heads=2, num_v_heads=4, head_dim=128, io_dtype="bf16",
+                        seed=31, init_std=0.05, ckpt_lists=ck)
+    elif case == "raw_gates":
+        base = I.make_pack([300, 77, 128, 5], num_k_heads=2, num_v_heads=4, head_dim=128,
+                           io_dtype="bf16", seed=32, init_std=0.02, ckpt_lists=[[128, 300], [], [64], [5]])
+        p = I.with_raw_gates(base, seed=5)
+    elif case == "ragged":
+        p = ragged
+    else:
+        p = I.make_pack([4096, 333], num_k_heads=4, num_v_heads=8, head_dim=128, io_dtype="bf16",
+                        seed=33, init_std=0.02, ckpt_lists=[[2048, 4096], [320]],
+                        decay_scale=I.LONG_DECAY_SCALE)
+    _assert_same(run(p, gdn.KERNEL_CHUNKED_PIPELINED), run(p, gdn.KERNEL_CHUNKED_THROUGHPUT))
+
+
+def test_automatic_choice_equals_forced_schedules(wave):
+    """The automatic result on the wave (throughput schedule) equals either forced
+    schedule bit for bit."""
+    torch = torch_cuda()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert gdn.gdn_chunked_schedule(wave.cu_seqlens, 32, sms) == gdn.KERNEL_CHUNKED_THROUGHPUT
     auto = run(wave)
-    for x, y in zip(auto, run(wave, gdn.KERNEL_CHUNKED_THROUGHPUT)):
-        np.testing.assert_array_equal(x, y)
+    _assert_same(auto, run(wave, gdn.KERNEL_CHUNKED_THROUGHPUT))
+    _assert_same(auto, run(wave, gdn.KERNEL_CHUNKED_PIPELINED))
+
+
+def test_auto_pack_vs_alone_bitwise_across_schedules():
+    """A pack for which the automatic choice takes the throughput schedule, against each
+    sampled prompt alone (for which it takes the pipelined one): identical o, checkpoints
+    and final states."""
+    torch = torch_cuda()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n_prompts = (6 * sms + 31) // 32
+    rng = np.random.default_rng(34)
+    lengths = [int(x) for x in rng.integers(1, 200, n_prompts)]
+    ck = [[q for q in range(64, n + 1, 64)] + ([n] if n % 64 else []) for n in lengths]
+    p = I.make_pack(lengths, num_k_heads=16, num_v_heads=32, head_dim=128, io_dtype="bf16",
+                    seed=35, init_std=0.02, ckpt_lists=ck)
+    assert gdn.gdn_chunked_schedule(p.cu_seqlens, 32, sms) == gdn.KERNEL_CHUNKED_THROUGHPUT
+    o, c, f = run(p)
+    for n in sorted({0, 1, n_prompts // 2, n_prompts - 1}):
+        s = I.sub_pack(p, [n])
+        assert gdn.gdn_chunked_schedule(s.cu_seqlens, 32, sms) == gdn.KERNEL_CHUNKED_PIPELINED
+        o1, c1, f1 = run(s)
+        np.testing.assert_array_equal(o[p.cu_seqlens[n]:p.cu_seqlens[n + 1]], o1)
+        np.testing.assert_array_equal(c[p.ckpt_cu[n]:p.ckpt_cu[n + 1]], c1)
+        np.testing.assert_array_equal(f[n], f1[0])
