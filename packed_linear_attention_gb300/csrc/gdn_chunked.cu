@@ -75,11 +75,21 @@ struct __align__(8) Smem {
   uint32_t tmem_base;
   float next_decay;  // e^{G_L} of the next chunk
 };
+// The warp that owns the gates: idle while thread 0 issues the chunk's last products (warp 1
+// folds the norms during the first product). (A second thread issuing the state update
+// alongside thread 0 was measured slower.)
+constexpr int kGateWarp = 2;
 
-// Wait for an mbarrier phase, uniformly across the block; false on timeout.
-__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t& phase) {
+// Waits (every thread, bounded) for the pending phase of an mbarrier, with one answer for
+// the whole block (false on a timeout). A phase that a thread saw complete advances its
+// `phase` and clears its `pending`; after a timeout both still name the pending phase, for
+// the cleanup.
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t& phase, bool& pending) {
   const bool ok = mbar_wait_bounded(bar, phase & 1u, kWaitLimit);
-  phase ^= 1u;
+  if (ok) {
+    phase ^= 1u;
+    pending = false;
+  }
   tc_fence_after();
   return !__syncthreads_or(!ok);
 }
@@ -110,7 +120,7 @@ __device__ __forceinline__ void issue_v(const ChunkedParams& P, uint8_t* sV, uin
 }
 
 
-// Loads the log-decays and betas of the chunk starting at token t0 (warp 0 only); with raw
+// Loads the log-decays and betas of the chunk starting at token t0 (one warp); with raw
 // gate inputs they are turned into gates here. Tokens past the chunk get a = beta = 0.
 __device__ __forceinline__ void load_gates(const float* ag, const float* bg, size_t stride,
                                            int t0, int len, int lane, bool raw,
@@ -249,15 +259,18 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
     tmem_alloc(&sm.tmem_base, TM_COLS);
     tmem_relinquish();
   }
-  // gates of chunk 0 (warp 0 keeps the next chunk's gates in registers)
+  // gate factors of chunk 0; the gate warp keeps the next chunk's gates in registers (every
+  // later chunk's factors are written while the previous chunk's last products run)
   float gnext[4] = {0.f, 0.f, 0.f, 0.f};
   const bool raw = p.gate_mode == 1;
   const float a_log = raw ? __ldg(p.a_log + h) : 0.f;
   const float dt_bias = raw ? __ldg(p.dt_bias + h) : 0.f;
-  if (warp == 0 && nchunks > 0) {
+  const float scale = p.scale;
+  if (warp == kGateWarp && nchunks > 0) {
     load_gates(ag, bg, p.hv_heads, 0, sd.len, lane, raw, a_log, dt_bias, gnext);
-    const float d = chunk_decay(gnext, lane);
+    const float d = write_gate_factors(Factors(sG), gnext, scale, lane);
     if (lane == 0) sm.next_decay = d;
+    if (nchunks > 1) load_gates(ag, bg, p.hv_heads, kC, sd.len, lane, raw, a_log, dt_bias, gnext);
   }
   tc_fence_before();
   __syncthreads();
@@ -292,27 +305,18 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
   uint32_t ph_mma = 0, ph_kq = 0, ph_v = 0;
   bool ok = true;
   const bool vz = sd.flags & kSeqZeroV;  // v taken as zero: no v copies at all
-  bool kq_inflight = nchunks > 0, v_inflight = nchunks > 0 && !vz;  // meaningful in thread 0
+  // copies and products in flight (meaningful in thread 0, which issues them)
+  bool kq_inflight = nchunks > 0, v_inflight = nchunks > 0 && !vz, mma_inflight = false;
   int c_next = sd.ckpt_begin;
-  const float scale = p.scale;
 
   for (int c = 0; c < nchunks && ok; ++c) {
     const int t0 = c * kC;
     const int L = min(kC, sd.len - t0);
 
-    // ---- (1) gates of this chunk from registers; fetch the next chunk's ------------------
-    if (warp == 0) {
-      write_gate_factors(Factors(sG), gnext, scale, lane);
-      if (c + 1 < nchunks)
-        load_gates(ag, bg, p.hv_heads, t0 + kC, sd.len, lane, raw, a_log, dt_bias, gnext);
-    }
-
     // ---- (2) wait for q, k, v; convert in place to fp16 (q, k normalised); zero past L ----
-    if (!(ok = wait_all(&sm.bar_kq, ph_kq))) break;
-    kq_inflight = false;
+    if (!(ok = wait_all(&sm.bar_kq, ph_kq, kq_inflight))) break;
     if (!vz) {
-      if (!(ok = wait_all(&sm.bar_v, ph_v))) break;
-      v_inflight = false;
+      if (!(ok = wait_all(&sm.bar_v, ph_v, v_inflight))) break;
     }
     if (tid == 0 && c + 1 < nchunks) {  // warm L2 with the next chunk's q, k, v
       const int nrow = sd.tok_start + t0 + kC;
@@ -376,6 +380,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
                    smem_desc_sw128(a0 + off, 16, 1024), idesc, s > 0);
       }
       mma_commit(&sm.bar_mma);
+      mma_inflight = true;
     }
     __syncwarp();
     if (warp == 1) {  // fold the norms into the per-token factors
@@ -408,7 +413,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
             (int)r < L && !vz ? bf16x8_to_half8(w[pass]) : zero;
       }
     }
-    if (!(ok = wait_all(&sm.bar_mma, ph_mma))) break;
+    if (!(ok = wait_all(&sm.bar_mma, ph_mma, mma_inflight))) break;
 
     // ---- (4) A (rows 0-63, fp32) and P (rows 64-127, fp16); Q~ = scale e^G Q / |q| over Q -
     {
@@ -510,9 +515,10 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
         mma_f16_ss(tbase + TM_R0, smem_desc_sw128(a0 + s * 2048, 16384, 1024),
                    smem_desc_sw128(b0 + s * 32, 16, 1024), idesc, s > 0);
       mma_commit(&sm.bar_mma);
+      mma_inflight = true;
     }
     __syncwarp();
-    if (!(ok = wait_all(&sm.bar_mma, ph_mma))) break;
+    if (!(ok = wait_all(&sm.bar_mma, ph_mma, mma_inflight))) break;
 
     // ---- (7) W^T -> smem (fp16, MN-major B: rows d_k, columns tokens) ---------------------------
     {
@@ -543,9 +549,10 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
         mma_f16_ts(tbase + TM_R0, tbase + TM_S16 + s * 8,
                    smem_desc_sw128(w0 + s * 2048, 16384, 1024), id_w, 1);
       mma_commit(&sm.bar_mma);
+      mma_inflight = true;
     }
     __syncwarp();
-    if (!(ok = wait_all(&sm.bar_mma, ph_mma))) break;
+    if (!(ok = wait_all(&sm.bar_mma, ph_mma, mma_inflight))) break;
     // V and T2 are consumed: fetch the next chunk's v now
     if (tid == 0 && c + 1 < nchunks && !vz) {
       issue_v(P, sV, &sm.bar_v, h, sd.tok_start + t0 + kC);
@@ -571,20 +578,13 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
         st_chunk(sWD, row, 32 * half + e, 128, x);
         st_chunk(sDp, row, 32 * half + e, 128, y);
       }
-      // total decay of the next chunk, for the state pre-scale after this chunk
-      if (warp == 0 && c + 1 < nchunks) {
-        const float d = chunk_decay(gnext, lane);
-        if (lane == 0) sm.next_decay = d;
-      }
     }
     publish_operands();
 
     // ---- (10) O^T = S16 Q~^T + D^T P^T -> R0;  S32 += D'^T K ----------------------------------
     if (tid == 0) {
       const uint32_t id_n64 = idesc_f16(128, 64, 0, 0);
-      const uint32_t id_n128 = idesc_f16(128, 128, 0, 1);
-      const uint32_t kq = smem_u32(sKQ), d0 = smem_u32(sWD), dp = smem_u32(sDp),
-                     p0 = smem_u32(sP);
+      const uint32_t kq = smem_u32(sKQ), d0 = smem_u32(sWD), p0 = smem_u32(sP);
 #pragma unroll
       for (int s = 0; s < kD / 16; ++s) {
         const uint32_t off = 8192 + (s >> 2) * 16384 + (s & 3) * 32;  // Q~ rows 64-127
@@ -595,14 +595,26 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       for (int s = 0; s < kC / 16; ++s)
         mma_f16_ss(tbase + TM_R0, smem_desc_sw128(d0 + s * 32, 16, 1024),
                    smem_desc_sw128(p0 + s * 32, 16, 1024), id_n64, 1);
+      const uint32_t id_n128 = idesc_f16(128, 128, 0, 1);
+      const uint32_t dp = smem_u32(sDp);
 #pragma unroll
       for (int s = 0; s < kC / 16; ++s)
         mma_f16_ss(tbase + TM_S32, smem_desc_sw128(dp + s * 32, 16, 1024),
                    smem_desc_sw128(kq + s * 2048, 16384, 1024), id_n128, 1);
       mma_commit(&sm.bar_mma);
+      mma_inflight = true;
     }
     __syncwarp();
-    if (!(ok = wait_all(&sm.bar_mma, ph_mma))) break;
+    // while the products run: the next chunk's gate factors (every read of this chunk's
+    // factors is behind the barrier above) and its total decay for the state pre-scale;
+    // then the gates of the chunk after it
+    if (warp == kGateWarp && c + 1 < nchunks) {
+      const float d = write_gate_factors(Factors(sG), gnext, scale, lane);
+      if (lane == 0) sm.next_decay = d;
+      if (c + 2 < nchunks)
+        load_gates(ag, bg, p.hv_heads, t0 + 2 * kC, sd.len, lane, raw, a_log, dt_bias, gnext);
+    }
+    if (!(ok = wait_all(&sm.bar_mma, ph_mma, mma_inflight))) break;
     // q and k are consumed: fetch the next chunk's
     if (tid == 0 && c + 1 < nchunks) {
       issue_kq(P, sKQ, &sm.bar_kq, hk, sd.tok_start + t0 + kC);
@@ -695,10 +707,10 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
   if (!ok) {
     if (tid == 0 && p.status) atomicExch(p.status, kStatusTimeout);
     // let products and copies still in flight land (bounded) before TMEM and shared
-    // memory are released: the MMA barrier's pending phase is the one that timed out
-    // (or was never waited), and thread 0 knows which tensor copies are outstanding
+    // memory are released: thread 0 knows what it has outstanding and the parity of each
+    // pending phase
     if (tid == 0) {
-      mbar_wait_bounded(&sm.bar_mma, ph_mma & 1u, kWaitLimit);
+      if (mma_inflight) mbar_wait_bounded(&sm.bar_mma, ph_mma & 1u, kWaitLimit);
       if (kq_inflight) mbar_wait_bounded(&sm.bar_kq, ph_kq & 1u, kWaitLimit);
       if (v_inflight) mbar_wait_bounded(&sm.bar_v, ph_v & 1u, kWaitLimit);
     }
