@@ -65,16 +65,16 @@ def algorithmic_flops(T, Hk, Hv, d, C=64):
 MEASURED_TRAFFIC = {
     "sources": {
         "packed_linear_attention_gb300/csrc/gdn_chunked.cu":
-            "5a6e10e8d948156e970ddb3baa150369e915b1f514019143948932143b0e2de2",
+            "d181c7cd8344ca25a6366906f3d1c5e2a5f17864b9d35f938f2f317c4d7aa082",
         "packed_linear_attention_gb300/csrc/gdn_chunk_util.cuh":
-            "d6648dbd67a086ebc38b79acdafced108e7505891e830e6a06f244b77dfc728d",
+            "737d3b2972ee3df89ae050f1aa64e1d19e3e4702bad88423184a73e0deb40c5f",
         "packed_linear_attention_gb300/csrc/ptx_sm103.cuh":
             "8498eb56a00787588a767b984c67c5d12a16d2004d612b5cfb5d46edd45ac374",
         "packed_linear_attention_gb300/csrc/gdn_tma.cu":
-            "6767277781b4efc4e5331a19f80a831271b6d2574cbfd7e56b833cd067998c0b",
+            "994011deeaff3fae57b896cea700b26197eca1b77724eb11980caf7be82efc42",
     },
     "read_bytes": 546.0e6,
-    "write_bytes": 359.1e6,
+    "write_bytes": 358.5e6,
 }
 
 
