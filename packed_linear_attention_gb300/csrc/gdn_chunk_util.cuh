@@ -155,6 +155,65 @@ __device__ __forceinline__ float write_gate_factors(const Factors& f, const floa
   return ptx::ex2(gl);
 }
 
+// q and k of one chunk (K rows 0-63, Q rows 64-127 of a 128B-swizzled tile whose two
+// 64-column regions start kRegionBytes apart) to fp16 in place (exact: bf16 values are fp16
+// values), with their inverse L2 norms into f.Rk / f.Rq (0 for rows past the chunk's L
+// tokens, which are zeroed). The norms are not applied to the tile: they are folded into
+// per-token factors. One group of 256 threads (gtid), 16 per row and 8 rows each.
+//  * Each row piece is stored as soon as it is converted: the stores need no norm.
+//  * The 8 rows' sums of squares are reduced over the 16 threads of a row by a
+//    reduce-scatter (each level keeps half of the partial sums), 8 shuffles in all; the
+//    thread pair (j, j^1) ends with the sum of row j >> 1, and thread j even writes its norm.
+// Both schedules of the chunked kernel call this one function, so that their norms, and
+// everything built from them, agree bit for bit.
+template <uint32_t kRegionBytes>
+__device__ __forceinline__ void convert_kq(uint8_t* sKQ, const Factors& f, int L, bool l2norm,
+                                           int gtid) {
+  const int j = gtid & 15, rsub = gtid >> 4;  // piece j of the row
+  const uint32_t reg = j >> 3, cc = j & 7;
+  auto at = [&](uint32_t r) {
+    return reinterpret_cast<uint4*>(sKQ + reg * kRegionBytes + (r >> 3) * 1024 + (r & 7) * 128 +
+                                    ((cc ^ (r & 7)) << 4));
+  };
+  uint4 w[8];
+#pragma unroll
+  for (int pass = 0; pass < 8; ++pass) w[pass] = *at(pass * 16 + rsub);
+  float ss[8];
+#pragma unroll
+  for (int pass = 0; pass < 8; ++pass) {
+    const uint32_t r = pass * 16 + rsub;
+    float x[8];
+    unpack_bf16x8(w[pass], x);
+    float a = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) a = __fmaf_rn(x[e], x[e], a);
+    ss[pass] = a;
+    *at(r) = (int)(r & 63) < L ? pack_half8(x) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  // reduce-scatter: 8 partial sums -> 4 (xor 8) -> 2 (xor 4) -> 1 (xor 2) -> full (xor 1)
+  const bool b8 = j & 8, b4 = j & 4, b2 = j & 2;
+  float s4[4], s2[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = b8 ? ss[i] : ss[4 + i];
+    s4[i] = __fadd_rn(b8 ? ss[4 + i] : ss[i], __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = b4 ? s4[i] : s4[2 + i];
+    s2[i] = __fadd_rn(b4 ? s4[2 + i] : s4[i], __shfl_xor_sync(0xffffffffu, send, 4));
+  }
+  float s1 = __fadd_rn(b2 ? s2[1] : s2[0],
+                       __shfl_xor_sync(0xffffffffu, b2 ? s2[0] : s2[1], 2));
+  s1 = __fadd_rn(s1, __shfl_xor_sync(0xffffffffu, s1, 1));
+  if (!(j & 1)) {
+    const int pass = j >> 1;  // 4 b8 + 2 b4 + b2
+    const uint32_t t = (uint32_t)(pass * 16 + rsub) & 63;
+    const float rn = (int)t < L ? (l2norm ? rsqrtf(s1 + kL2NormEps) : 1.f) : 0.f;
+    (pass < 4 ? f.Rk : f.Rq)[t] = rn;
+  }
+}
+
 // One 16 x 8 output tile D = sum_k Ablk[r0.., k] * Bblk[k.., n0..] over k in [k_lo, k_hi)
 // (multiples of 8) on one warp, tf32 warp MMAs. Both matrices fp32 with row strides lda/ldb.
 __device__ __forceinline__ void tile_mm(float (&d)[4], const float* Am, int lda, int r0,

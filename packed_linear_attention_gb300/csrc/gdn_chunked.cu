@@ -327,46 +327,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
         tma_prefetch_l2_2d(&P.tv, h * kD + 64 * r, nrow);
       }
     }
-    {
-      // raw bf16 -> fp16 in place (exact); rows past the chunk are zeroed. The norms are
-      // not applied to the tiles: they are folded into per-token factors below.
-      const int j = tid & 15, rsub = tid >> 4;  // 16 threads per row, chunk j of the row
-      const uint32_t reg = j >> 3, cc = j & 7;
-      const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-      uint4 w[8];
-#pragma unroll
-      for (int pass = 0; pass < 8; ++pass) {   // K rows 0-63, Q rows 64-127
-        const uint32_t r = pass * 16 + rsub;
-        w[pass] = *reinterpret_cast<const uint4*>(sKQ + reg * 16384 + (r >> 3) * 1024 +
-                                                  (r & 7) * 128 + ((cc ^ (r & 7)) << 4));
-      }
-      float ss[8];
-#pragma unroll
-      for (int pass = 0; pass < 8; ++pass) {
-        float x[8];
-        unpack_bf16x8(w[pass], x);
-        float a = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) a += x[e] * x[e];
-        ss[pass] = a;
-        w[pass] = pack_half8(x);  // exact: bf16 values are fp16 values
-      }
-#pragma unroll
-      for (int off = 8; off > 0; off >>= 1)
-#pragma unroll
-        for (int pass = 0; pass < 8; ++pass) ss[pass] += __shfl_xor_sync(0xffffffffu, ss[pass], off);
-#pragma unroll
-      for (int pass = 0; pass < 8; ++pass) {
-        const uint32_t r = pass * 16 + rsub, t = r & 63;
-        const bool live = (int)t < L;
-        if (j == 0) {
-          const float rn = live ? (p.l2norm ? rsqrtf(ss[pass] + kL2NormEps) : 1.f) : 0.f;
-          (pass < 4 ? sRk : sRq)[t] = rn;
-        }
-        *reinterpret_cast<uint4*>(sKQ + reg * 16384 + (r >> 3) * 1024 + (r & 7) * 128 +
-                                  ((cc ^ (r & 7)) << 4)) = live ? w[pass] : zero;
-      }
-    }
+    convert_kq<16384>(sKQ, Factors(sG), L, p.l2norm != 0, tid);  // with the norms
     publish_operands();
 
     // ---- (3) M1: [K; Q] K^T -> R0 (128 x 64) ------------------------------------------------

@@ -258,50 +258,6 @@ __device__ void invert_merge(const float* A, float* T, float* X, uint8_t* T1, ui
   named_sync(kBarPrep, kGroup);
 }
 
-// q and k of one chunk to fp16 in place (exact: bf16 values are fp16 values) with their
-// inverse L2 norms into f.Rk / f.Rq; rows past the chunk's L tokens are zeroed. The norms
-// are not applied to the tiles: they are folded into per-token factors. One warp group
-// (gtid 0-255), 16 threads per row.
-__device__ __forceinline__ void convert_kq(uint8_t* sKQ, const Factors& f, int L, bool l2norm,
-                                           int gtid) {
-  const int j = gtid & 15, rsub = gtid >> 4;  // chunk j of the row
-  const uint32_t reg = j >> 3, cc = j & 7;
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  uint4 w[8];
-#pragma unroll
-  for (int pass = 0; pass < 8; ++pass) {   // K rows 0-63, Q rows 64-127
-    const uint32_t r = pass * 16 + rsub;
-    w[pass] = *reinterpret_cast<const uint4*>(sKQ + reg * kRegion + (r >> 3) * 1024 +
-                                              (r & 7) * 128 + ((cc ^ (r & 7)) << 4));
-  }
-  float ss[8];
-#pragma unroll
-  for (int pass = 0; pass < 8; ++pass) {
-    float x[8];
-    unpack_bf16x8(w[pass], x);
-    float a = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) a += x[e] * x[e];
-    ss[pass] = a;
-    w[pass] = pack_half8(x);
-  }
-#pragma unroll
-  for (int off = 8; off > 0; off >>= 1)
-#pragma unroll
-    for (int pass = 0; pass < 8; ++pass) ss[pass] += __shfl_xor_sync(0xffffffffu, ss[pass], off);
-#pragma unroll
-  for (int pass = 0; pass < 8; ++pass) {
-    const uint32_t r = pass * 16 + rsub, t = r & 63;
-    const bool live = (int)t < L;
-    if (j == 0) {
-      const float rn = live ? (l2norm ? rsqrtf(ss[pass] + kL2NormEps) : 1.f) : 0.f;
-      (pass < 4 ? f.Rk : f.Rq)[t] = rn;
-    }
-    *reinterpret_cast<uint4*>(sKQ + reg * kRegion + (r >> 3) * 1024 + (r & 7) * 128 +
-                              ((cc ^ (r & 7)) << 4)) = live ? w[pass] : zero;
-  }
-}
-
 // v of one chunk to fp16 in place (exact); rows past the chunk's L tokens are zeroed. One
 // warp group (gtid 0-255).
 __device__ __forceinline__ void convert_v(uint8_t* sV, int L, int gtid) {
@@ -585,7 +541,8 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
       const int bb = cc & 1;
       if (!group_wait(sm, B_KQ0 + bb, (cc >> 1) & 1, kBarChain, leader)) return false;
       const Factors fb(reinterpret_cast<float*>(smem + OFF_VEC + bb * 2048));
-      convert_kq(smem + OFF_KQ + bb * kKQW, fb, min(kC, sd.len - cc * kC), p.l2norm != 0, ctid);
+      convert_kq<kRegion>(smem + OFF_KQ + bb * kKQW, fb, min(kC, sd.len - cc * kC),
+                          p.l2norm != 0, ctid);
       fence_proxy_async_smem();
       named_sync(kBarChain, kGroup);
       if (leader) mbar_arrive(&sm.bar[B_CONV0 + bb]);
