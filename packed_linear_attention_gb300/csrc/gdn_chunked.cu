@@ -166,8 +166,14 @@ __device__ __forceinline__ void invert_diag_blocks(const float* A, float* T, int
   for (int i = 0; i < 16; ++i) T[(o + i) * kLd + o + j] = x[i];
 }
 
-// Step 2 of the inverse (all warps), after the diagonal blocks are in T.
-__device__ void invert_merge(const float* A, float* T, float* X, int tid) {
+// Step 2 of the inverse (all warps), after the diagonal blocks are in T; it also writes the
+// fp16 operands T1 = T diag(c1) and T2 = T diag(c2) (128B-swizzled 64 x 64 tiles, zero
+// above the diagonal). T1/T2 share their shared memory with A, so they are written once A
+// has been read for the last time (by X = A[32:64, 0:32] T[0:32, 0:32]): the last product's
+// block straight from its accumulator, every other block from T. Ends before the tiles are
+// published to the tensor cores.
+__device__ void invert_merge(const float* A, float* T, float* X, uint8_t* T1, uint8_t* T2,
+                             const float* c1, const float* c2, int tid) {
   const int warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
   // 16 -> 32: T[16b+16.., 16b..] = -T22 (A21 T11) for b = 0, 2; warps 0-3, one 8-column slice
   if (warp < 4) {
@@ -192,14 +198,39 @@ __device__ void invert_merge(const float* A, float* T, float* X, int tid) {
     tile_store(X, kLdX, r0, n0, d, 1.f, gid, tig);
   }
   __syncthreads();
-  {
+  {  // A is dead from here: T[32:64, 0:32] = -T[32:64, 32:64] X straight into T1/T2
     const int mt = warp >> 2, nt = warp & 3;
     const int r0 = 16 * mt, n0 = 8 * nt;
     float y[4] = {0.f, 0.f, 0.f, 0.f};
     tile_mm(y, T + 32 * kLd + 32, kLd, r0, X, kLdX, n0, 0, mt == 0 ? 16 : 32, gid, tig);
-    tile_store(T, kLd, 32 + r0, n0, y, -1.f, gid, tig);
+    tile_store_t12(T1, T2, 32 + r0, n0, y, c1, c2, gid, tig);
   }
-  __syncthreads();
+  {  // the other blocks from T: 16 columns of one row per thread
+    const int i = tid >> 2, jb = (tid & 3) * 16;
+    if (i < 32 || jb >= 32) {
+#pragma unroll
+      for (int h8 = 0; h8 < 16; h8 += 8) {
+        float x1[8], x2[8];
+#pragma unroll
+        for (int q4 = 0; q4 < 8; q4 += 4) {
+          const int j = jb + h8 + q4;
+          const float4 tv = *reinterpret_cast<const float4*>(T + i * kLd + j);
+          const float4 gv = *reinterpret_cast<const float4*>(c1 + j);
+          const float4 bv = *reinterpret_cast<const float4*>(c2 + j);
+          const float t4[4] = {tv.x, tv.y, tv.z, tv.w}, g4[4] = {gv.x, gv.y, gv.z, gv.w},
+                      b4[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+          for (int f = 0; f < 4; ++f) {
+            const float tij = j + f <= i ? t4[f] : 0.f;
+            x1[q4 + f] = tij * g4[f];
+            x2[q4 + f] = tij * b4[f];
+          }
+        }
+        st_chunk(T1, i, jb + h8, 64, x1);
+        st_chunk(T2, i, jb + h8, 64, x2);
+      }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
@@ -440,31 +471,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       }
     }
     __syncthreads();
-    invert_merge(sA, sT, sXs, tid);
-    {
-      const int i = tid >> 2, jb = (tid & 3) * 16;
-#pragma unroll
-      for (int h8 = 0; h8 < 16; h8 += 8) {
-        float x1[8], x2[8];
-#pragma unroll
-        for (int q4 = 0; q4 < 8; q4 += 4) {
-          const int j = jb + h8 + q4;
-          const float4 tv = *reinterpret_cast<const float4*>(sT + i * kLd + j);
-          const float4 bv = *reinterpret_cast<const float4*>(sB + j);
-          const float4 gv = *reinterpret_cast<const float4*>(sBG + j);
-          const float t4[4] = {tv.x, tv.y, tv.z, tv.w}, b4[4] = {bv.x, bv.y, bv.z, bv.w},
-                      g4[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-          for (int f = 0; f < 4; ++f) {
-            const float tij = j + f <= i ? t4[f] : 0.f;
-            x2[q4 + f] = tij * b4[f];
-            x1[q4 + f] = tij * g4[f];
-          }
-        }
-        st_chunk(sT1, i, jb + h8, 64, x1);
-        st_chunk(sT2, i, jb + h8, 64, x2);
-      }
-    }
+    invert_merge(sA, sT, sXs, sT1, sT2, sBG, sB, tid);
     publish_operands();
 
     // ---- (6) M2: W^T = K^T T1^T -> R0 (128 x 64) -----------------------------------------------

@@ -203,21 +203,6 @@ __device__ __forceinline__ void invert_diag_blocks(const float* A, float* T, uin
   }
 }
 
-// A negated 16 x 8 accumulator tile of T at (r0, n0) into T1 and T2 (column pairs as half2).
-__device__ __forceinline__ void tile_store_t12(uint8_t* T1, uint8_t* T2, int r0, int n0,
-                                               const float (&d)[4], const float* c1,
-                                               const float* c2, int gid, int tig) {
-  const int col = n0 + 2 * tig;
-  const float g0 = c1[col], g1 = c1[col + 1], b0 = c2[col], b1 = c2[col + 1];
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    const uint32_t off = sw128_offset(r0 + gid + 8 * hh, col, 64);
-    const float x0 = -d[2 * hh], x1 = -d[2 * hh + 1];
-    *reinterpret_cast<uint32_t*>(T1 + off) = pack_half2(x0 * g0, x1 * g1);
-    *reinterpret_cast<uint32_t*>(T2 + off) = pack_half2(x0 * b0, x1 * b1);
-  }
-}
-
 // Step 2 (all prep warps), after the diagonal blocks are in T. Ends with T1/T2 published
 // to the tensor cores.
 __device__ void invert_merge(const float* A, float* T, float* X, uint8_t* T1, uint8_t* T2,
