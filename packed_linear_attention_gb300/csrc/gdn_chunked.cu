@@ -149,10 +149,11 @@ __device__ __forceinline__ void load_gates(const float* ag, const float* bg, siz
 // diagonal, so their tf32 rounding leaves T within about 1e-6 relative, far below the fp16
 // rounding of the operands built from T. Only the lower triangle and the unit diagonal of
 // T are written; blocks of T above the diagonal are never read.
-// Step 1 of the inverse, run by warps 0 and 1 while the other warps do independent work.
-__device__ __forceinline__ void invert_diag_blocks(const float* A, float* T, int tid) {
-  const int warp = tid >> 5, lane = tid & 31;
-  const int o = 16 * (2 * warp + (lane >> 4)), j = lane & 15;
+// Step 1 of the inverse: one warp inverts diagonal blocks 2 pair and 2 pair + 1 (pair 0 or 1;
+// lanes 0-15 the first block, 16-31 the second) while the other warps do independent work.
+__device__ __forceinline__ void invert_diag_blocks(const float* A, float* T, int pair,
+                                                   int lane) {
+  const int o = 16 * (2 * pair + (lane >> 4)), j = lane & 15;
   float x[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) x[i] = i == j ? 1.f : 0.f;
@@ -448,13 +449,18 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       }
     }
     tc_fence_before();
-    __syncthreads();
 
     // ---- (5) T = (I + A)^-1; T1 = T diag(beta e^G), T2 = T diag(beta) (fp16) -----------------
-    if (warp < 2) {
-      invert_diag_blocks(sA, sT, tid);
-    } else {  // Q~ rows while the diagonal blocks are inverted (M1 has consumed Q)
-      for (int idx = tid - 64; idx < 1024; idx += kThreads - 64) {
+    // The diagonal 16 x 16 blocks of A lie in rows that the inverting warps have just written
+    // themselves: warp 0 wrote rows 0-31, columns 0-31 (blocks 0 and 1) and warp 5 rows 32-63,
+    // columns 32-63 (blocks 2 and 3). They invert them at once, without waiting for the other
+    // warps, which scale Q~ meanwhile (M1 has consumed Q).
+    if (warp == 0 || warp == 5) {
+      __syncwarp();
+      invert_diag_blocks(sA, sT, warp == 0 ? 0 : 1, lane);
+    } else {
+      const int rank = warp < 5 ? warp - 1 : warp - 2;  // 0-5 over warps 1-4, 6, 7
+      for (int idx = 32 * rank + lane; idx < 1024; idx += kThreads - 64) {
         const uint32_t t = idx >> 4, j = idx & 15, rr = 64 + t;
         const uint32_t reg = j >> 3, cc = j & 7;
         uint4* ptr = reinterpret_cast<uint4*>(sKQ + reg * 16384 + (rr >> 3) * 1024 +

@@ -178,12 +178,12 @@ __device__ __forceinline__ void commit(Smem& sm, int i) {
 // Every block of T is also written, as soon as it is known, into the fp16 operands
 // T1 = T diag(c1) and T2 = T diag(c2) (column factors c1, c2; 128B-swizzled 64 x 64 tiles
 // whose blocks above the diagonal are zero).
-// Step 1, run by prep warps 0 and 1 while the other prep warps do independent work.
+// Step 1: one prep warp inverts diagonal blocks 2 pair and 2 pair + 1 (pair 0 or 1; lanes
+// 0-15 the first block, 16-31 the second) while the other prep warps do independent work.
 __device__ __forceinline__ void invert_diag_blocks(const float* A, float* T, uint8_t* T1,
                                                    uint8_t* T2, const float* c1,
-                                                   const float* c2, int tid) {
-  const int warp = tid >> 5, lane = tid & 31;
-  const int o = 16 * (2 * warp + (lane >> 4)), j = lane & 15;
+                                                   const float* c2, int pair, int lane) {
+  const int o = 16 * (2 * pair + (lane >> 4)), j = lane & 15;
   float x[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) x[i] = i == j ? 1.f : 0.f;
@@ -424,13 +424,17 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
         }
       }
       tc_fence_before();
-      named_sync(kBarPrep, kGroup);
 
       // ---- (6) T = (I + A)^-1; Q~ = scale e^G Q / |q| over Q meanwhile ------------------------
-      if (warp < 2) {
-        invert_diag_blocks(sA, sT, sT1, sT2, f.BG, f.B, tid);
+      // The diagonal 16 x 16 blocks of A lie in rows that the inverting warps have just
+      // written themselves (warp 0: rows and columns 0-31, blocks 0 and 1; warp 5: rows and
+      // columns 32-63, blocks 2 and 3), so they start without waiting for the other warps.
+      if (warp == 0 || warp == 5) {
+        __syncwarp();
+        invert_diag_blocks(sA, sT, sT1, sT2, f.BG, f.B, warp == 0 ? 0 : 1, lane);
       } else {  // M1 has consumed Q
-        for (int idx = tid - 64; idx < 1024; idx += kGroup - 64) {
+        const int rank = warp < 5 ? warp - 1 : warp - 2;  // 0-5 over warps 1-4, 6, 7
+        for (int idx = 32 * rank + lane; idx < 1024; idx += kGroup - 64) {
           const uint32_t t = idx >> 4, j = idx & 15, rr = 64 + t;
           const uint32_t reg = j >> 3, cc = j & 7;
           uint4* ptr = reinterpret_cast<uint4*>(sKQ + reg * kRegion + (rr >> 3) * 1024 +
