@@ -54,12 +54,13 @@ constexpr int kThreads = 256;
 constexpr uint32_t OFF_KQ = 0;         // K (rows 0-63) and Q (rows 64-127): 2 regions x 16 KB
 constexpr uint32_t OFF_V = 32768;      // V: 2 regions x 8 KB
 constexpr uint32_t OFF_P = 49152;      // P: 64 x 64 fp16
-constexpr uint32_t OFF_A = 57344;      // A fp32 [64][68] -> T1 | T2 -> D' -> o staging
-constexpr uint32_t OFF_T2 = OFF_A + 8192;
+constexpr uint32_t OFF_A = 57344;      // A fp32 [64][68] -> T1 (first 8 KB) -> D' -> o staging
 constexpr uint32_t OFF_WD = 75776;     // T fp32 [64][68] -> W^T -> D
 constexpr uint32_t OFF_XS = OFF_WD + 17408;  // inverse scratch: 32 x 36 fp32
-constexpr uint32_t OFF_VEC = OFF_XS + 5120;  // per-token gate factors: 5 x 64 fp32
-constexpr uint32_t SMEM_USED = OFF_VEC + 2048;
+constexpr uint32_t OFF_VEC = OFF_XS + 5120;  // per-token gate factors: 8 x 64 fp32
+constexpr uint32_t OFF_T2 = OFF_VEC + 2048;  // T2 (fp16 64 x 64), a region of its own
+static_assert(OFF_T2 % 1024 == 0, "shared-memory map");
+constexpr uint32_t SMEM_USED = OFF_T2 + 8192;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
 
 constexpr uint32_t TM_R0 = 0, TM_S16 = 64, TM_S32 = 128, TM_COLS = 256;
@@ -169,10 +170,11 @@ __device__ __forceinline__ void invert_diag_blocks(const float* A, float* T, int
 
 // Step 2 of the inverse (all warps), after the diagonal blocks are in T; it also writes the
 // fp16 operands T1 = T diag(c1) and T2 = T diag(c2) (128B-swizzled 64 x 64 tiles, zero
-// above the diagonal). T1/T2 share their shared memory with A, so they are written once A
-// has been read for the last time (by X = A[32:64, 0:32] T[0:32, 0:32]): the last product's
-// block straight from its accumulator, every other block from T. Ends before the tiles are
-// published to the tensor cores.
+// above the diagonal). T1 shares its shared memory with rows 0-30 of A, which the 16 -> 32
+// level reads for the last time; T2 has a region of its own. So the blocks of T1/T2 that
+// are final after that level are written while the products of the 32 -> 64 level run,
+// and that level's last product goes straight from its accumulator into T1/T2. Ends
+// before the tiles are published to the tensor cores.
 __device__ void invert_merge(const float* A, float* T, float* X, uint8_t* T1, uint8_t* T2,
                              const float* c1, const float* c2, int tid) {
   const int warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
@@ -191,22 +193,13 @@ __device__ void invert_merge(const float* A, float* T, float* X, uint8_t* T1, ui
   __syncthreads();
   // 32 -> 64: X = A[32:64, 0:32] T[0:32, 0:32], then T[32:64, 0:32] = -T[32:64, 32:64] X;
   // eight 16 x 8 tiles, one per warp; zero blocks of the triangular factors are skipped
+  const int mt = warp >> 2, nt = warp & 3;
+  const int r0 = 16 * mt, n0 = 8 * nt;
   {
-    const int mt = warp >> 2, nt = warp & 3;
-    const int r0 = 16 * mt, n0 = 8 * nt;
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     tile_mm(d, A + 32 * kLd, kLd, r0, T, kLd, n0, nt >= 2 ? 16 : 0, 32, gid, tig);
-    tile_store(X, kLdX, r0, n0, d, 1.f, gid, tig);
-  }
-  __syncthreads();
-  {  // A is dead from here: T[32:64, 0:32] = -T[32:64, 32:64] X straight into T1/T2
-    const int mt = warp >> 2, nt = warp & 3;
-    const int r0 = 16 * mt, n0 = 8 * nt;
-    float y[4] = {0.f, 0.f, 0.f, 0.f};
-    tile_mm(y, T + 32 * kLd + 32, kLd, r0, X, kLdX, n0, 0, mt == 0 ? 16 : 32, gid, tig);
-    tile_store_t12(T1, T2, 32 + r0, n0, y, c1, c2, gid, tig);
-  }
-  {  // the other blocks from T: 16 columns of one row per thread
+    // while the warp MMAs run: every block of T1/T2 but T[32:64, 0:32], from T (16
+    // columns of one row per thread)
     const int i = tid >> 2, jb = (tid & 3) * 16;
     if (i < 32 || jb >= 32) {
 #pragma unroll
@@ -231,6 +224,13 @@ __device__ void invert_merge(const float* A, float* T, float* X, uint8_t* T1, ui
         st_chunk(T2, i, jb + h8, 64, x2);
       }
     }
+    tile_store(X, kLdX, r0, n0, d, 1.f, gid, tig);
+  }
+  __syncthreads();
+  {  // T[32:64, 0:32] = -T[32:64, 32:64] X straight into T1/T2
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+    tile_mm(y, T + 32 * kLd + 32, kLd, r0, X, kLdX, n0, 0, mt == 0 ? 16 : 32, gid, tig);
+    tile_store_t12(T1, T2, 32 + r0, n0, y, c1, c2, gid, tig);
   }
 }
 
