@@ -124,6 +124,15 @@ gdn_status gdn_pool_info(gdn_handle* handle, void** host_ptr, size_t* bytes);
  * automatic choice differs; the token-serial kernel agrees with them to rounding. Errors: INVALID_ARGUMENT. */
 gdn_status gdn_set_kernel_preference(gdn_handle* handle, int32_t preference);
 
+/* Test hook for the device-side timeout path (hook 1; 0 = off, the default). While it is
+ * set, the chunked tensor-core kernels leave out every unit's first q/k tile copy, so each
+ * unit's first copy wait runs out after its time bound (about one second of polling) with
+ * no fault: the kernel records GDN_ERR_DEVICE_TIMEOUT in the status word that
+ * gdn_read_device_status returns, lets every copy and product it did issue land, frees its
+ * tensor memory and returns. The outputs of such a call are undefined; the CUDA context
+ * stays usable. The token-serial kernel ignores the hook. Errors: INVALID_ARGUMENT. */
+gdn_status gdn_set_test_hook(gdn_handle* handle, int32_t hook);
+
 /* The chunked kernel's schedule that the automatic choice takes for a pack of `num_seqs`
  * prompts (cu_seqlens_host: prefix sums, as for gdn_prefill_packed) with `num_v_heads`
  * value heads on a GPU with `num_sms` SMs: *schedule = 2 (pipelined) or 3 (throughput),

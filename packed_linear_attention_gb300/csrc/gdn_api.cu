@@ -49,6 +49,7 @@ struct gdn_handle {
   StagingSlot slots[kStagingSlots];
   int next_slot = 0;
   int32_t kernel_pref = 0;
+  int32_t test_hook = 0;  // gdn_set_test_hook
   // the owned prefill stream: at most one prefill in flight on it
   cudaStream_t prefill_stream = nullptr;
   cudaEvent_t prefill_ready = nullptr;  // caller stream -> prefill stream
@@ -329,6 +330,12 @@ gdn_status gdn_set_kernel_preference(gdn_handle* h, int32_t pref) {
   return GDN_OK;
 }
 
+gdn_status gdn_set_test_hook(gdn_handle* h, int32_t hook) {
+  if (!h || hook < 0 || hook > 1) return GDN_ERR_INVALID_ARGUMENT;
+  h->test_hook = hook;
+  return GDN_OK;
+}
+
 gdn_status gdn_chunked_schedule(int32_t num_seqs, const int32_t* cu, int32_t num_v_heads,
                                 int32_t num_sms, int32_t* schedule) {
   if (num_seqs < 0 || (num_seqs > 0 && !cu) || num_v_heads < 1 || num_sms < 1 || !schedule)
@@ -444,7 +451,9 @@ int launch_prefill(KernelFamily fam, const gdn_handle* h, const gdn_config* cfg,
                    void* stream) {
   if (fam == kChunked) {
     const int schedule = h && h->kernel_pref >= 2 ? h->kernel_pref : gdn::kChunkedAuto;
-    return gdn::launch_chunked_prefill(pa, T, schedule, load, stream);
+    gdn::PrefillArgs args = pa;
+    args.test_skip_first_copy = h ? h->test_hook : 0;
+    return gdn::launch_chunked_prefill(args, T, schedule, load, stream);
   }
   return gdn::launch_recurrent_prefill(pa, cfg->head_dim_k, cfg->io_dtype == GDN_BF16, stream);
 }

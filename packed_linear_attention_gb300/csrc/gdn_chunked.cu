@@ -283,7 +283,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       prefetch_tmap(&P.tq);
       prefetch_tmap(&P.tk);
       prefetch_tmap(&P.tv);
-      issue_kq(P, sKQ, &sm.bar_kq, hk, sd.tok_start);
+      if (!p.test_skip_first_copy) issue_kq(P, sKQ, &sm.bar_kq, hk, sd.tok_start);
       if (!(sd.flags & kSeqZeroV)) issue_v(P, sV, &sm.bar_v, h, sd.tok_start);
     }
   }
@@ -338,7 +338,8 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
   bool ok = true;
   const bool vz = sd.flags & kSeqZeroV;  // v taken as zero: no v copies at all
   // copies and products in flight (meaningful in thread 0, which issues them)
-  bool kq_inflight = nchunks > 0, v_inflight = nchunks > 0 && !vz, mma_inflight = false;
+  bool kq_inflight = nchunks > 0 && !p.test_skip_first_copy;
+  bool v_inflight = nchunks > 0 && !vz, mma_inflight = false;
   int c_next = sd.ckpt_begin;
 
   for (int c = 0; c < nchunks && ok; ++c) {

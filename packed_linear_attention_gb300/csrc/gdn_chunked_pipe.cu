@@ -101,17 +101,19 @@ struct __align__(8) Smem {
 };
 
 // Waits (every thread of a group) for phase `parity` of mbarrier `i`; gives up after the
-// poll limit or once the other group has given up. The answer is made uniform across the
-// group, and one thread records the observed completion.
+// poll or time limit or once the other group has given up. The answer is made uniform
+// across the group, and one thread records the observed completion.
 __device__ __forceinline__ bool group_wait(Smem& sm, int i, uint32_t parity, uint32_t bar_id,
                                            bool leader, bool extra_fail = false) {
   bool ok = false;
+  WaitClock clk;
   for (uint32_t n = 0; n < kWaitLimit; ++n) {
     if (mbar_try_wait(&sm.bar[i], parity)) {
       ok = true;
       break;
     }
     if ((n & 63u) == 63u && sm.abort) break;
+    if (clk.expired(n)) break;
   }
   tc_fence_after();
   const bool fail = named_any(bar_id, kGroup, !ok || extra_fail);
@@ -121,12 +123,14 @@ __device__ __forceinline__ bool group_wait(Smem& sm, int i, uint32_t parity, uin
 
 // Single-thread bounded wait (used by a group leader before it issues products).
 __device__ __forceinline__ bool leader_wait(Smem& sm, int i, uint32_t parity) {
+  WaitClock clk;
   for (uint32_t n = 0; n < kWaitLimit; ++n) {
     if (mbar_try_wait(&sm.bar[i], parity)) {
       tc_fence_after();
       return true;
     }
     if ((n & 63u) == 63u && sm.abort) break;
+    if (clk.expired(n)) break;
   }
   return false;
 }
@@ -309,7 +313,7 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
       prefetch_tmap(&P.tq);
       prefetch_tmap(&P.tk);
       prefetch_tmap(&P.tv);
-      issue_kq(P, sm, smem + OFF_KQ, 0, hk, sd.tok_start);
+      if (!p.test_skip_first_copy) issue_kq(P, sm, smem + OFF_KQ, 0, hk, sd.tok_start);
       if (!(sd.flags & kSeqZeroV)) issue_v(P, sm, sV, h, sd.tok_start);
       if (nchunks > 1) issue_kq(P, sm, smem + OFF_KQ + kKQW, 1, hk, sd.tok_start + kC);
     }

@@ -58,6 +58,9 @@ struct PrefillArgs {
   int32_t gate_mode;      // 0: a, beta as given; 1: raw projections (see gate_from_raw)
   const float* a_log;     // [Hv] (gate_mode 1)
   const float* dt_bias;   // [Hv] (gate_mode 1)
+  // Test hook (gdn_set_test_hook): the chunked kernels leave out every unit's first q/k
+  // copy, so that its first bounded wait runs out and the timeout path runs.
+  int32_t test_skip_first_copy = 0;
 };
 
 struct DecodeArgs {

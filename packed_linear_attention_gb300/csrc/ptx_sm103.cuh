@@ -101,12 +101,38 @@ __device__ __forceinline__ bool mbar_wait_sleep_bounded(uint64_t* bar, uint32_t 
   return false;
 }
 
-// Bounded wait: gives up after `limit` polls (each poll may itself suspend briefly) and
-// returns false, so a lost arrival can never hang the GPU.
+// The GPU's nanosecond clock (%globaltimer).
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Time bound of every bounded wait: about one second.
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+// Tracks how long a bounded wait has polled: the clock is read once every 256 failed polls,
+// so a wait that completes soon never reads it.
+struct WaitClock {
+  uint64_t t0 = 0;
+  __device__ __forceinline__ bool expired(uint32_t n) {
+    if ((n & 255u) != 255u) return false;
+    const uint64_t t = global_ns();
+    if (t0 == 0) t0 = t;
+    return t - t0 > kWaitNs;
+  }
+};
+
+// Bounded wait: gives up after `limit` polls (each poll may itself suspend briefly) or
+// about kWaitNs of polling, whichever comes first, and returns false, so a lost arrival
+// can never hang the GPU.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   uint32_t limit) {
-  for (uint32_t i = 0; i < limit; ++i)
+  WaitClock clk;
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (clk.expired(i)) return false;
+  }
   return false;
 }
 

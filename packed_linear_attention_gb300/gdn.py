@@ -45,7 +45,7 @@ EXPORTS = (
     "gdn_prefill_packed_noalloc", "gdn_prefill_packed_async", "gdn_prefill_async_query",
     "gdn_prefill_async_wait", "gdn_prefill_async_join", "gdn_prefill_split_workspace_size",
     "gdn_prefill_packed_split", "gdn_prefill_packed_host", "gdn_prefill_host_workspace_size",
-    "gdn_chunked_schedule",
+    "gdn_chunked_schedule", "gdn_set_test_hook",
 )
 
 
@@ -95,6 +95,7 @@ def load(path: str = LIB_PATH):
             "gdn_pool_info": (I32, [P, ctypes.POINTER(P), ctypes.POINTER(SZ)]),
             "gdn_set_kernel_preference": (I32, [P, I32]),
             "gdn_chunked_schedule": (I32, [I32, IP, I32, I32, IP]),
+            "gdn_set_test_hook": (I32, [P, I32]),
             "gdn_prefill_workspace_size": (I32, [CFG, I32, IP, IP, ctypes.POINTER(SZ)]),
             "gdn_prefill_packed": (I32, [P, CFG, I32, IP, P, P, P, P, P, P, IP, IP, P, P, P,
                                          P, SZ, P]),
@@ -202,6 +203,12 @@ def gdn_pool_info(handle: int) -> tuple[int, int]:
 def gdn_set_kernel_preference(handle: int, preference: int) -> None:
     _check(load().gdn_set_kernel_preference(handle, int(preference)),
            "gdn_set_kernel_preference")
+
+
+def gdn_set_test_hook(handle: int, hook: int) -> None:
+    """1: the chunked kernels leave out every unit's first q/k copy, so that its first
+    bounded wait runs out (the device timeout path, without a fault); 0: off."""
+    _check(load().gdn_set_test_hook(handle, int(hook)), "gdn_set_test_hook")
 
 
 def gdn_chunked_schedule(cu_seqlens, num_v_heads: int, num_sms: int) -> int:

@@ -218,3 +218,10 @@ def test_chunked_schedule_choice(lib):
         with pytest.raises(gdn.GdnError) as e:
             choose(*bad)
         assert e.value.status == gdn.GDN_ERR_INVALID_ARGUMENT
+
+
+def test_test_hook_validation(lib):
+    for hook in (0, 1):
+        with pytest.raises(gdn.GdnError) as e:
+            gdn.gdn_set_test_hook(None, hook)  # no handle
+        assert e.value.status == gdn.GDN_ERR_INVALID_ARGUMENT
