@@ -52,6 +52,15 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs p) {
   const T* q = static_cast<const T*>(p.q) + ((size_t)b * p.hk_heads + hk) * D;
   const T* k = static_cast<const T*>(p.k) + ((size_t)b * p.hk_heads + hk) * D;
 
+  // this thread's state chunks first: their loads overlap warp 0's q/k work below
+  const int r = tid >> 2, sub = tid & 3, row = row0 + r;
+  const size_t slot = (size_t)p.slot[b];
+  float4* srow = reinterpret_cast<float4*>(p.pool + ((slot * p.hv_heads + h) * D + row) * D);
+  float4 S[kVec];
+#pragma unroll
+  for (int m = 0; m < kVec; ++m) S[m] = srow[sub + 4 * m];
+  float ga = p.a[(size_t)b * p.hv_heads + h], bb = p.beta[(size_t)b * p.hv_heads + h];
+  const float vi = ld_f32(static_cast<const T*>(p.v) + ((size_t)b * p.hv_heads + h) * D + row);
   if (warp == 0) {
     float qv[D / 32], kv[D / 32], qq = 0.f, kk = 0.f;
 #pragma unroll
@@ -74,16 +83,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs p) {
       sk[lane + 32 * e] = kv[e] * ks;
     }
   }
-  const int r = tid >> 2, sub = tid & 3, row = row0 + r;
-  const size_t slot = (size_t)p.slot[b];
-  float4* srow = reinterpret_cast<float4*>(p.pool + ((slot * p.hv_heads + h) * D + row) * D);
-  float4 S[kVec];
-#pragma unroll
-  for (int m = 0; m < kVec; ++m) S[m] = srow[sub + 4 * m];
-  float ga = p.a[(size_t)b * p.hv_heads + h], bb = p.beta[(size_t)b * p.hv_heads + h];
   if (p.gate_mode == 1) gate_from_raw(p.a_log[h], p.dt_bias[h], ga, bb);
   const float g = __expf(ga);
-  const float vi = ld_f32(static_cast<const T*>(p.v) + ((size_t)b * p.hv_heads + h) * D + row);
   __syncthreads();
 
   const float4* kr = reinterpret_cast<const float4*>(sk);
