@@ -65,16 +65,16 @@ def algorithmic_flops(T, Hk, Hv, d, C=64):
 MEASURED_TRAFFIC = {
     "sources": {
         "packed_linear_attention_gb300/csrc/gdn_chunked.cu":
-            "d181c7cd8344ca25a6366906f3d1c5e2a5f17864b9d35f938f2f317c4d7aa082",
+            "02e97d1f2106a972db8e1e65fd3d606f6b9a6832ca221341a3a1e219473a746f",
         "packed_linear_attention_gb300/csrc/gdn_chunk_util.cuh":
-            "737d3b2972ee3df89ae050f1aa64e1d19e3e4702bad88423184a73e0deb40c5f",
+            "67714127fd97adc366d0856df63937eb34567895fa4509124b60e8115c8f7079",
         "packed_linear_attention_gb300/csrc/ptx_sm103.cuh":
-            "8498eb56a00787588a767b984c67c5d12a16d2004d612b5cfb5d46edd45ac374",
+            "eec246cde63c45bba67348c03196e8ffe0d0a609f014f7a80db6a0d89f8598e8",
         "packed_linear_attention_gb300/csrc/gdn_tma.cu":
             "994011deeaff3fae57b896cea700b26197eca1b77724eb11980caf7be82efc42",
     },
     "read_bytes": 546.0e6,
-    "write_bytes": 358.5e6,
+    "write_bytes": 357.0e6,
 }
 
 
