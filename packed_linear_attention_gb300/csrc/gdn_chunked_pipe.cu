@@ -388,7 +388,15 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
       if (!(ok = group_wait(sm, B_M1, c & 1, kBarPrep, leader))) break;
 
       // ---- (5) A (rows 0-63, fp32) and P (rows 64-127, fp16) ----------------------------------
-      {
+      // Warps whose 32 x 32 block lies above the diagonal (rows 0-31 of A or of P, columns
+      // 32-63) compute nothing: that block of A is never read, that block of P is zero.
+      if (half == 1 && (sub == 0 || sub == 2)) {
+        if (sub == 2) {
+          const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) st_chunk(sP, row - 64, 32 + e, 64, z);
+        }
+      } else {
         uint32_t r[32];
         tmem_ld32(t_lane + TM_M + 32 * half, r);
         tmem_ld_wait();
