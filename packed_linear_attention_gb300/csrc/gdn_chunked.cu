@@ -23,14 +23,17 @@
 // Throughput schedule: per CTA (256 threads, 8 warps, two CTAs per SM) one unit, the
 // phases of each chunk in sequence; the two CTAs of an SM hide each other's latencies.
 // The pipelined schedule (gdn_chunked_pipe.cu) computes the same chunk algebra with one
-// 16-warp CTA per SM; launch_chunked_prefill picks between them.
+// 16-warp CTA per SM, rounding every value the same way (the code they share is in
+// gdn_chunk_util.cuh), so their results are bit-identical; launch_chunked_prefill picks
+// between them.
 //   TMEM (256 columns): [0,64) R0 = the current product (fp32); [64,128) S16 = fp16 state
 //   copy (A operand of the state products); [128,256) S32 = fp32 state, accumulated in
 //   place by the update product.
 //   Shared memory (128B-swizzled fp16 tiles, see ptx_sm103.cuh): raw bf16 q/k/v arrive by
 //   TMA and are converted in place; the next chunk's v is fetched as soon as the current
 //   one is consumed, q/k as soon as the last product of the chunk has read them.
-// Every mbarrier wait is bounded; a timeout is reported through the status word.
+// Every mbarrier wait is bounded (a poll count and about one second); a timeout is
+// reported through the status word.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>

@@ -1,4 +1,5 @@
-// gdn_chunked.cu — chunked gated-delta-rule prefill on the tcgen05 tensor cores (sm_103a).
+// gdn_chunked_pipe.cu — chunked gated-delta-rule prefill on the tcgen05 tensor cores
+// (sm_103a), pipelined schedule.
 //
 // Method (Gated Delta Networks, Yang, Kautz & Hatamizadeh, 2024, in its chunked UT/WY
 // form). Per (prompt, value head) unit the state S (d_v x d_k = 128 x 128, fp32) is carried
@@ -32,9 +33,11 @@
 //   TMEM (512 columns): [0,128) S32 fp32 state; [128,192) S16 fp16 copy (A operand);
 //   [192,256) the prep group's product; [256,512) two blocks [O^T | U^T], one per buffer:
 //   the chain's single product S16 [Q~; -W]^T starts O^T and turns U^T into D^T.
-// Every mbarrier wait is bounded and gives up early once the other group has; a timeout is
-// reported through the status word and every copy and product still in flight is waited
-// for (bounded) before TMEM is released.
+// Results are bit-identical to the throughput schedule's (gdn_chunked.cu): both round every
+// value the same way, with the code they share in gdn_chunk_util.cuh.
+// Every mbarrier wait is bounded (a poll count and about one second) and gives up early
+// once the other group has; a timeout is reported through the status word and every copy
+// and product still in flight is waited for (bounded) before TMEM is released.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
