@@ -443,6 +443,34 @@ def run_secondary(torch, gdn, I, h, stream, flush, hbm_gbs):
     dbytes = B * 32 * 128 * 128 * 4 * 2 + B * (2 * 16 * 128 * 2 + 2 * 32 * 128 * 2 + 2 * 32 * 4)
     out["decode_32seq"] = {"sequences": B, "us": ms * 1e3, "achieved_gbs": dbytes / (ms / 1e3) / 1e9,
                            "frac_hbm": dbytes / (ms / 1e3) / 1e9 / hbm_gbs}
+    # a mixed step: the prompt slices under the 1,024-token budget and the 32 decode tokens,
+    # (a) as a prefill plus a separate decode launch, (b) as one prefill pack in which each
+    # decode token is a one-token segment resuming from its state (the states laid out as
+    # the pack's initial-state array; no gather from a pool is timed)
+    pre = ms_step.prefill
+    pbuf = gdn.to_device(pre)
+    ms_two = _time_events(torch, lambda: (gdn.prefill(h, pbuf, stream), gdn.gdn_decode_step(
+        h, cfg, B, q, k, v, a, beta, pool, B, slots, o, stream)), stream, flush)
+    lengths = list(pre.lengths) + [1] * B
+    both = I.Pack(name="mixed_one_pack",
+                  cu_seqlens=np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32),
+                  q=np.concatenate([pre.q, ms_step.dec_q]), k=np.concatenate([pre.k, ms_step.dec_k]),
+                  v=np.concatenate([pre.v, ms_step.dec_v]), a=np.concatenate([pre.a, ms_step.dec_a]),
+                  beta=np.concatenate([pre.beta, ms_step.dec_beta]),
+                  init=np.concatenate([np.zeros((pre.num_seqs, 32, 128, 128), np.float32),
+                                       ms_step.dec_states]),
+                  ckpt_cu=np.zeros(len(lengths) + 1, np.int32), ckpt_pos=np.zeros(0, np.int32),
+                  num_k_heads=16, num_v_heads=32, head_dim=128, io_dtype="bf16",
+                  scale=128 ** -0.5)
+    obuf = gdn.to_device(both)
+    ms_one = _time_events(torch, lambda: gdn.prefill(h, obuf, stream), stream, flush)
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    out["mixed_step"] = {
+        "prompt_tokens": pre.total_tokens, "decode_tokens": B,
+        "prefill_plus_decode_us": ms_two * 1e3, "one_pack_us": ms_one * 1e3,
+        "one_pack_schedule": "throughput" if gdn.gdn_chunked_schedule(
+            both.cu_seqlens, 32, sms) == gdn.KERNEL_CHUNKED_THROUGHPUT else "pipelined"}
+    del pbuf, obuf
     return out
 
 
