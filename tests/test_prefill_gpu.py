@@ -268,3 +268,18 @@ def test_auto_pack_vs_alone_bitwise_across_schedules():
         np.testing.assert_array_equal(o[p.cu_seqlens[n]:p.cu_seqlens[n + 1]], o1)
         np.testing.assert_array_equal(c[p.ckpt_cu[n]:p.ckpt_cu[n + 1]], c1)
         np.testing.assert_array_equal(f[n], f1[0])
+
+
+@pytest.mark.parametrize("pref", KERNELS + CHUNKED)
+@pytest.mark.parametrize("hk,hv", [(4, 4), (2, 4), (1, 4), (2, 8)])
+def test_gqa_group_sizes(pref, hk, hv):
+    """Value head h reads key head h // (H_v / H_k): groups of 1 (4/4), 2 (2/4) and 4 (1/4,
+    2/8), every value head of the pack against the oracle (a wrong key-head index fails at
+    once)."""
+    torch_cuda()
+    lengths = [130, 64, 1, 200]
+    ck = [[64, 128, 130], [64], [1], [192, 200]]
+    p = I.make_pack(lengths, num_k_heads=hk, num_v_heads=hv, head_dim=128, io_dtype="bf16",
+                    seed=50 + hk + hv, init_std=0.02, ckpt_lists=ck)
+    got = run(p, pref)
+    compare_units(p, got, list(range(len(lengths))), list(range(hv)))
