@@ -65,9 +65,9 @@ def algorithmic_flops(T, Hk, Hv, d, C=64):
 MEASURED_TRAFFIC = {
     "sources": {
         "packed_linear_attention_gb300/csrc/gdn_chunked.cu":
-            "02e97d1f2106a972db8e1e65fd3d606f6b9a6832ca221341a3a1e219473a746f",
+            "063c679e6977bd8dd3e3a6a49df8b1937e7ecc7ef9f92521b5a4173e3750a832",
         "packed_linear_attention_gb300/csrc/gdn_chunk_util.cuh":
-            "67714127fd97adc366d0856df63937eb34567895fa4509124b60e8115c8f7079",
+            "8dd59f6de8c27e6acd1f85a116ee1ac986c9965147a2dc19d3da679a025b2184",
         "packed_linear_attention_gb300/csrc/ptx_sm103.cuh":
             "eec246cde63c45bba67348c03196e8ffe0d0a609f014f7a80db6a0d89f8598e8",
         "packed_linear_attention_gb300/csrc/gdn_tma.cu":

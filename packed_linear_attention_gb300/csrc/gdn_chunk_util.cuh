@@ -214,17 +214,31 @@ __device__ __forceinline__ void convert_kq(uint8_t* sKQ, const Factors& f, int L
   }
 }
 
-// One 16 x 8 output tile D = sum_k Ablk[r0.., k] * Bblk[k.., n0..] over k in [k_lo, k_hi)
-// (multiples of 8) on one warp, tf32 warp MMAs. Both matrices fp32 with row strides lda/ldb.
+// One 16 x 8 output tile D += sum_k Ablk[r0.., k] * Bblk[k.., n0..] over k in [k_lo, k_hi)
+// (multiples of 8, at most 32 wide) on one warp, tf32 warp MMAs. Both matrices fp32 with
+// row strides lda/ldb. Each 8-wide k step goes into a zeroed tile of its own and the partial
+// tiles are added in a fixed order, (p0 + p1) + (p2 + p3): the steps run side by side
+// instead of as one chain of dependent warp MMAs, whose latency dominates products this
+// small (measured: 2% on a single 32K-token prompt, neutral elsewhere).
 __device__ __forceinline__ void tile_mm(float (&d)[4], const float* Am, int lda, int r0,
                                         const float* Bm, int ldb, int n0, int k_lo, int k_hi,
                                         int gid, int tig) {
-  for (int k = k_lo; k < k_hi; k += 8) {
-    const float a[4] = {Am[(r0 + gid) * lda + k + tig], Am[(r0 + gid + 8) * lda + k + tig],
-                        Am[(r0 + gid) * lda + k + tig + 4], Am[(r0 + gid + 8) * lda + k + tig + 4]};
-    const float b[2] = {Bm[(k + tig) * ldb + n0 + gid], Bm[(k + tig + 4) * ldb + n0 + gid]};
-    ptx::mma_tf32_f(d, a, b);
+  float p[4][4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) p[s][e] = 0.f;
+    const int k = k_lo + 8 * s;
+    if (k < k_hi) {
+      const float a[4] = {Am[(r0 + gid) * lda + k + tig], Am[(r0 + gid + 8) * lda + k + tig],
+                          Am[(r0 + gid) * lda + k + tig + 4],
+                          Am[(r0 + gid + 8) * lda + k + tig + 4]};
+      const float b[2] = {Bm[(k + tig) * ldb + n0 + gid], Bm[(k + tig + 4) * ldb + n0 + gid]};
+      ptx::mma_tf32_f(p[s], a, b);
+    }
   }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) d[e] += (p[0][e] + p[1][e]) + (p[2][e] + p[3][e]);
 }
 
 // Stores a 16 x 8 accumulator tile (optionally negated) at (r0, n0) of an fp32 matrix.
