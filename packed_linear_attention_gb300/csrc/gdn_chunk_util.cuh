@@ -128,12 +128,6 @@ __device__ __forceinline__ float gate_scan(const float (&g)[4], int lane, float&
   return __shfl_sync(0xffffffffu, a1, 31);  // padded tokens add nothing
 }
 
-// e^{G_L} of a chunk from its gates (one warp): the state's decay over the chunk.
-__device__ __forceinline__ float chunk_decay(const float (&g)[4], int lane) {
-  float a0, a1;
-  return ptx::ex2(gate_scan(g, lane, a0, a1));
-}
-
 // The gate factors of one chunk from its gates (one warp, tokens lane and lane + 32); the
 // norms are folded in later. Returns e^{G_L}.
 __device__ __forceinline__ float write_gate_factors(const Factors& f, const float (&g)[4],

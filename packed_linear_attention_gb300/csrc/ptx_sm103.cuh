@@ -79,28 +79,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// try_wait with a suspend-time hint: the thread sleeps until the phase completes or about
-// `hint_ns` nanoseconds pass, instead of spinning on the issue slots.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
-                                                    uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-      " selp.b32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded sleeping wait: at most `limit` tries of about `hint_ns` each, then false.
-__device__ __forceinline__ bool mbar_wait_sleep_bounded(uint64_t* bar, uint32_t parity,
-                                                        uint32_t hint_ns, uint32_t limit) {
-  for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_try_wait_sleep(bar, parity, hint_ns)) return true;
-  return false;
-}
-
 // The GPU's nanosecond clock (%globaltimer).
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
