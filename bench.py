@@ -67,9 +67,9 @@ MEASURED_TRAFFIC = {
         "packed_linear_attention_gb300/csrc/gdn_chunked.cu":
             "063c679e6977bd8dd3e3a6a49df8b1937e7ecc7ef9f92521b5a4173e3750a832",
         "packed_linear_attention_gb300/csrc/gdn_chunk_util.cuh":
-            "8dd59f6de8c27e6acd1f85a116ee1ac986c9965147a2dc19d3da679a025b2184",
+            "e0236f840d351cdce6c937270bc974f932a44168f7bb01f7583bd2cd4def152d",
         "packed_linear_attention_gb300/csrc/ptx_sm103.cuh":
-            "eec246cde63c45bba67348c03196e8ffe0d0a609f014f7a80db6a0d89f8598e8",
+            "8d1cb743537c6ed6b8227be46d40fc68426452810e0b9a00659c0e8ba1f86b1f",
         "packed_linear_attention_gb300/csrc/gdn_tma.cu":
             "994011deeaff3fae57b896cea700b26197eca1b77724eb11980caf7be82efc42",
     },
