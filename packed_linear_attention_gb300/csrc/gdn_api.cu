@@ -704,6 +704,10 @@ struct VSeq {
 gdn::ChunkLoad vseq_load(const std::vector<VSeq>& vs, int32_t units_per_prompt) {
   gdn::ChunkLoad l;
   for (const VSeq& x : vs) {
+    if (x.len <= 1) {
+      l.short_units += units_per_prompt;
+      continue;
+    }
     const int32_t c = (x.len + 63) / 64;
     l.total += (int64_t)c * units_per_prompt;
     l.longest = std::max(l.longest, c);

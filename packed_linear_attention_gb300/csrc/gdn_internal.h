@@ -113,16 +113,24 @@ int launch_decode(const DecodeArgs& a, int head_dim, bool bf16, void* stream);
 enum ChunkedSchedule : int { kChunkedAuto = 0, kChunkedPipelined = 2, kChunkedThroughput = 3 };
 constexpr int kThroughputCtasPerSM = 2;  // resident throughput CTAs per SM
 
-// Chunk counts of a pack's work list: over all units, and of the longest unit.
+// Chunk counts of a pack's work list: over all units, and of the longest unit; and the units
+// of prompts with at most one token, which close the longest-first work list and run in a
+// launch of their own (launch_short_units).
 struct ChunkLoad {
   int64_t total = 0;
   int32_t longest = 0;
+  int64_t short_units = 0;
 };
 // The load of a pack of prompts (cu: host prefix sums) with `units_per_prompt` units each.
 inline ChunkLoad chunk_load(const int32_t* cu, int32_t num_seqs, int32_t units_per_prompt) {
   ChunkLoad l;
   for (int32_t n = 0; n < num_seqs; ++n) {
-    const int32_t c = (cu[n + 1] - cu[n] + 63) / 64;
+    const int32_t len = cu[n + 1] - cu[n];
+    if (len <= 1) {
+      l.short_units += units_per_prompt;
+      continue;
+    }
+    const int32_t c = (len + 63) / 64;
     l.total += (int64_t)c * units_per_prompt;
     if (c > l.longest) l.longest = c;
   }
@@ -134,6 +142,9 @@ int launch_chunked_throughput(const PrefillArgs& a, int64_t total_tokens, void* 
 int launch_chunked_pipelined(const PrefillArgs& a, int64_t total_tokens, void* stream);
 int launch_chunked_prefill(const PrefillArgs& a, int64_t total_tokens, int schedule,
                            const ChunkLoad& load, void* stream);
+// Units a.units[0 .. a.num_units) of prompts with one token or none (bf16 io, d = 128): the
+// single update on CUDA cores, four 128-thread blocks per unit (gdn_decode.cu).
+int launch_short_units(const PrefillArgs& a, void* stream);
 
 // 2D bf16 tensor maps (64 x 64 boxes, 128-byte swizzle, zero fill past the last row) over
 // q, k (H_k * d columns) and v (H_v * d columns) with total_tokens rows (gdn_tma.cu).

@@ -91,8 +91,20 @@ int launch_chunked_prefill(const PrefillArgs& a, int64_t total_tokens, int sched
     }
     schedule = plan_schedule(load, n);
   }
-  return schedule == kChunkedThroughput ? launch_chunked_throughput(a, total_tokens, stream)
-                                        : launch_chunked_pipelined(a, total_tokens, stream);
+  // prompts with one token or none close the longest-first work list: their units get a
+  // launch of their own, the rest the chunked kernel
+  const int32_t tail = (int32_t)load.short_units;
+  PrefillArgs head = a, rest = a;
+  head.num_units = a.num_units - tail;
+  rest.units = a.units + head.num_units;
+  rest.num_units = tail;
+  if (head.num_units > 0) {
+    const int e = schedule == kChunkedThroughput
+                      ? launch_chunked_throughput(head, total_tokens, stream)
+                      : launch_chunked_pipelined(head, total_tokens, stream);
+    if (e != 0) return e;
+  }
+  return tail > 0 ? launch_short_units(rest, stream) : 0;
 }
 
 }  // namespace gdn
