@@ -139,7 +139,9 @@ gdn_status gdn_set_test_hook(gdn_handle* handle, int32_t hook);
  * the gdn_set_kernel_preference codes. The choice is the smaller of two estimates from
  * per-chunk costs measured on GB300 (6.4 us per chunk for a pipelined unit on its own SM,
  * 9.5 us for a throughput unit alone on its SM, 11.6 us for one of two sharing an SM), over
- * W = the chunks of all (prompt, value head) units and Lmax = the chunks of the longest:
+ * W = the chunks of all (prompt, value head) units and Lmax = the chunks of the longest,
+ * prompts of one token or none left out (their units always run in a launch of their own,
+ * with the decode step's arithmetic):
  *   pipelined:  6.4 max(Lmax, W / num_sms)
  *   throughput: max(9.5 Lmax, 11.6 W / (2 num_sms)).
  * Both schedules give bit-identical results; only the time differs. Host-only arithmetic,
