@@ -315,7 +315,10 @@ typedef struct {
 } gdn_prefill_buffers;
 
 /* gdn_prefill_packed for a pack whose inputs and outputs live in host memory. The prompts
- * are processed in groups of `group_prompts`. A group's rows of q, k, v, a, beta and its
+ * are processed in groups of `group_prompts`, except that with group_prompts > 1 (and more
+ * than two prompts) the first and the last group hold one prompt each, which shortens the
+ * copy-in that precedes the first prefill and the copy-out that follows the last one. A
+ * group's rows of q, k, v, a, beta and its
  * initial states are copied into `device` on the handle's copy-in stream; its prefill runs
  * on `stream` (exactly as gdn_prefill_packed over that group); its o rows, checkpoints and
  * final states are copied back into `host` on the handle's copy-out stream. The copies of
@@ -326,10 +329,10 @@ typedef struct {
  * gdn_prefill_packed would take (their inputs are overwritten with the host inputs).
  * Validation is that of gdn_prefill_packed on the whole pack and on `device`. Errors: also
  * INVALID_ARGUMENT for a missing host array or group_prompts < 1, UNSUPPORTED for more than
- * 64 groups. Results equal gdn_prefill_packed's on each group's sub-pack (the kernel
- * schedule is chosen per group, so with the automatic choice they may differ from a
- * whole-pack call by rounding). The workspace holds every group's work list, uploaded in
- * one copy ahead of the bulk copies (gdn_prefill_host_workspace_size). */
+ * 64 groups. Results equal gdn_prefill_packed's on the whole pack bit for bit (a prompt's
+ * results do not depend on its pack, and both chunked schedules agree bit for bit). The
+ * workspace holds every group's work list, uploaded in one copy ahead of the bulk copies
+ * (gdn_prefill_host_workspace_size). */
 /* Device workspace bytes that gdn_prefill_packed_host needs for this pack and group size
  * (the work lists of all groups). A multiple of 256. */
 gdn_status gdn_prefill_host_workspace_size(const gdn_config* cfg, int32_t num_seqs,

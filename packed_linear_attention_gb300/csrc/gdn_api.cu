@@ -531,14 +531,25 @@ gdn_status plan_groups(const gdn_handle* h, const gdn_config* cfg, int32_t num_s
   if (num_seqs < 1 || !cu || cu[0] != 0) return GDN_ERR_INVALID_ARGUMENT;
   for (int32_t n = 0; n < num_seqs; ++n)
     if (cu[n + 1] < cu[n]) return GDN_ERR_INVALID_ARGUMENT;
-  const int32_t groups = (num_seqs + group_prompts - 1) / group_prompts;
+  // Group boundaries. With groups of more than one prompt the first and the last group hold
+  // one prompt each: the copy-in before the first prefill and the prefill and copy-out after
+  // the last copy-in are the parts of the call that nothing overlaps.
+  std::vector<int32_t> bounds{0};
+  int32_t mid_end = num_seqs;
+  if (group_prompts > 1 && num_seqs > 2) {
+    bounds.push_back(1);
+    mid_end = num_seqs - 1;
+  }
+  while (bounds.back() < mid_end) bounds.push_back(std::min(mid_end, bounds.back() + group_prompts));
+  if (mid_end < num_seqs) bounds.push_back(num_seqs);
+  const int32_t groups = (int32_t)bounds.size() - 1;
   if (groups > kMaxHostGroups) return GDN_ERR_UNSUPPORTED;
   out->clear();
   *total = 0;
   for (int32_t g = 0; g < groups; ++g) {
     HostGroup G;
-    G.n0 = g * group_prompts;
-    G.n1 = std::min(num_seqs, G.n0 + group_prompts);
+    G.n0 = bounds[g];
+    G.n1 = bounds[g + 1];
     G.c0 = ckpt_cu ? ckpt_cu[G.n0] : 0;
     G.c1 = ckpt_cu ? ckpt_cu[G.n1] : 0;
     if (G.c1 < G.c0) return GDN_ERR_INVALID_ARGUMENT;

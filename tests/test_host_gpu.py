@@ -1,7 +1,8 @@
 """gdn_prefill_packed_host: inputs and outputs in pinned host memory, processed in groups of
 prompts whose copies overlap their neighbours' prefill. Results against gdn_prefill_packed
-on the same pack (bitwise when the kernel schedule is fixed, since each group is a sub-pack
-and results do not depend on packing) and against the oracle."""
+on the same pack (bitwise, also under the automatic choice: results do not depend on
+packing, and both chunked schedules agree bit for bit) and against the oracle. With groups
+of more than one prompt the first and last groups hold one prompt each.""" 
 import numpy as np
 import pytest
 
@@ -50,8 +51,8 @@ def _host_run(pack, group, pref=gdn.KERNEL_AUTO):
 
 
 @pytest.mark.parametrize("group", [1, 3, 16])
-@pytest.mark.parametrize("pref", [gdn.KERNEL_CHUNKED_PIPELINED, gdn.KERNEL_CHUNKED_THROUGHPUT,
-                                  gdn.KERNEL_RECURRENT])
+@pytest.mark.parametrize("pref", [gdn.KERNEL_AUTO, gdn.KERNEL_CHUNKED_PIPELINED,
+                                  gdn.KERNEL_CHUNKED_THROUGHPUT, gdn.KERNEL_RECURRENT])
 def test_host_prefill_equals_device_prefill(group, pref):
     lengths = [300, 64, 0, 1, 700, 129, 65]
     ck = [[64, 300], [64], [], [1], [256, 512, 700], [128], []]
