@@ -315,8 +315,8 @@ typedef struct {
 } gdn_prefill_buffers;
 
 /* gdn_prefill_packed for a pack whose inputs and outputs live in host memory. The prompts
- * are processed in groups of `group_prompts`, except that with group_prompts > 1 (and more
- * than two prompts) the first and the last group hold one prompt each, which shortens the
+ * are processed in groups of up to `group_prompts`: the groups grow 1, 2, 4, ... prompts up
+ * to group_prompts at the start and shrink the same way at the end, which keeps short the
  * copy-in that precedes the first prefill and the copy-out that follows the last one. A
  * group's rows of q, k, v, a, beta and its
  * initial states are copied into `device` on the handle's copy-in stream; its prefill runs

@@ -531,17 +531,32 @@ gdn_status plan_groups(const gdn_handle* h, const gdn_config* cfg, int32_t num_s
   if (num_seqs < 1 || !cu || cu[0] != 0) return GDN_ERR_INVALID_ARGUMENT;
   for (int32_t n = 0; n < num_seqs; ++n)
     if (cu[n + 1] < cu[n]) return GDN_ERR_INVALID_ARGUMENT;
-  // Group boundaries. With groups of more than one prompt the first and the last group hold
-  // one prompt each: the copy-in before the first prefill and the prefill and copy-out after
-  // the last copy-in are the parts of the call that nothing overlaps.
-  std::vector<int32_t> bounds{0};
-  int32_t mid_end = num_seqs;
-  if (group_prompts > 1 && num_seqs > 2) {
-    bounds.push_back(1);
-    mid_end = num_seqs - 1;
+  // Group sizes: 1, 2, 4, ... up to group_prompts at the start, group_prompts in the middle,
+  // and the same ramp reversed at the end. The copy-in before the first prefill and the
+  // prefill and copy-out after the last copy-in are the parts of the call that nothing
+  // overlaps, so the end groups are small; the middle ones are large, for fewer copies.
+  std::vector<int32_t> sizes;
+  {
+    std::vector<int32_t> ramp;
+    for (int64_t g = 1; g < group_prompts; g *= 2) ramp.push_back((int32_t)g);
+    int32_t left = num_seqs;
+    std::vector<int32_t> head, tail;
+    for (int32_t g : ramp) {
+      if (left <= 2 * g) break;
+      head.push_back(g);
+      tail.push_back(g);
+      left -= 2 * g;
+    }
+    for (int32_t g : head) sizes.push_back(g);
+    while (left > 0) {
+      const int32_t g = std::min(left, group_prompts);
+      sizes.push_back(g);
+      left -= g;
+    }
+    for (auto it = tail.rbegin(); it != tail.rend(); ++it) sizes.push_back(*it);
   }
-  while (bounds.back() < mid_end) bounds.push_back(std::min(mid_end, bounds.back() + group_prompts));
-  if (mid_end < num_seqs) bounds.push_back(num_seqs);
+  std::vector<int32_t> bounds{0};
+  for (int32_t g : sizes) bounds.push_back(bounds.back() + g);
   const int32_t groups = (int32_t)bounds.size() - 1;
   if (groups > kMaxHostGroups) return GDN_ERR_UNSUPPORTED;
   out->clear();

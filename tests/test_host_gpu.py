@@ -1,8 +1,8 @@
 """gdn_prefill_packed_host: inputs and outputs in pinned host memory, processed in groups of
 prompts whose copies overlap their neighbours' prefill. Results against gdn_prefill_packed
 on the same pack (bitwise, also under the automatic choice: results do not depend on
-packing, and both chunked schedules agree bit for bit) and against the oracle. With groups
-of more than one prompt the first and last groups hold one prompt each.""" 
+packing, and both chunked schedules agree bit for bit) and against the oracle. Group sizes
+ramp up 1, 2, 4, ... at the start and down at the end."""
 import numpy as np
 import pytest
 
