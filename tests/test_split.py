@@ -95,10 +95,12 @@ def test_split_raw_gates_vs_oracle():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("pref", [gdn.KERNEL_CHUNKED_PIPELINED, gdn.KERNEL_CHUNKED_THROUGHPUT])
+@pytest.mark.parametrize("pref", [gdn.KERNEL_AUTO, gdn.KERNEL_CHUNKED_PIPELINED,
+                                  gdn.KERNEL_CHUNKED_THROUGHPUT])
 def test_whole_prompts_match_gdn_prefill_packed_bitwise(pref):
     """Prompts no longer than the segment length are computed exactly as by
-    gdn_prefill_packed (same kernel schedule)."""
+    gdn_prefill_packed (under the automatic choice too: both chunked schedules agree bit
+    for bit)."""
     lengths = [300, 64, 1, 255]
     ck = [[128, 300], [64], [], [192]]
     p = I.make_pack(lengths, num_k_heads=2, num_v_heads=4, head_dim=128, io_dtype="bf16",
