@@ -71,7 +71,7 @@ MEASURED_TRAFFIC = {
         "packed_linear_attention_gb300/csrc/ptx_sm103.cuh":
             "8d1cb743537c6ed6b8227be46d40fc68426452810e0b9a00659c0e8ba1f86b1f",
         "packed_linear_attention_gb300/csrc/gdn_tma.cu":
-            "994011deeaff3fae57b896cea700b26197eca1b77724eb11980caf7be82efc42",
+            "a436f19726f8b42f0f87a2c8198857b0854bf15e7d0b549380f7dd32d6fd4129",
     },
     "read_bytes": 546.0e6,
     "write_bytes": 357.0e6,
