@@ -283,3 +283,23 @@ def test_gqa_group_sizes(pref, hk, hv):
                     seed=50 + hk + hv, init_std=0.02, ckpt_lists=ck)
     got = run(p, pref)
     compare_units(p, got, list(range(len(lengths))), list(range(hv)))
+
+
+def test_many_short_prompts():
+    """512 prompts of 0-130 tokens (8,192 units, 8 full waves of SMs): both schedules agree
+    bit for bit, the automatic result equals them, and sampled prompts and heads match the
+    oracle (the first, the last, empty and one-token prompts among them)."""
+    torch_cuda()
+    rng = np.random.default_rng(77)
+    lengths = [int(x) for x in rng.integers(0, 131, 512)]
+    lengths[5], lengths[6], lengths[7] = 0, 1, 64
+    ck = [[q for q in range(64, n + 1, 64)] + ([n] if n % 64 and n > 0 else []) for n in lengths]
+    p = I.make_pack(lengths, num_k_heads=8, num_v_heads=16, head_dim=128, io_dtype="bf16",
+                    seed=78, init_std=0.02, ckpt_lists=ck)
+    a = run(p, gdn.KERNEL_CHUNKED_PIPELINED)
+    b = run(p, gdn.KERNEL_CHUNKED_THROUGHPUT)
+    c = run(p)
+    for x, y, z in zip(a, b, c):
+        np.testing.assert_array_equal(x, y)
+        np.testing.assert_array_equal(x, z)
+    compare_units(p, b, [0, 5, 6, 7, 255, 511], [0, 1, 14, 15], per_item=False)
