@@ -15,10 +15,11 @@ def test_reference_arm_json_line():
     lines = [ln for ln in out.splitlines() if ln.startswith("{")]
     assert len(lines) == 1, out
     j = json.loads(lines[0])
-    with open(os.path.join(ROOT, "BASELINE.json")) as f:
-        metric = json.load(f)["metric"]
+    sys.path.insert(0, ROOT)
+    import bench
     assert j["impl"] == "reference"
-    assert j["metric"] == metric and j["unit"] == "tokens/s" and j["higher_is_better"] is True
+    assert j["metric"] == bench.METRIC and j["unit"] == bench.UNIT == "tokens/s"
+    assert j["higher_is_better"] is True
     assert j["n_gpus"] == 1 and j["steps"] == 3 and j["warmup"] == 3
     assert j["value"] > 0 and j["ms_per_step"] > 0 and j["vs_baseline"] is None
     assert j["data"] == "synthetic" and j["scaling"] == "weak"
