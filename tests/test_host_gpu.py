@@ -64,11 +64,12 @@ def test_host_prefill_equals_device_prefill(group, pref):
         np.testing.assert_array_equal(x, y)
 
 
-def test_host_prefill_wave_vs_oracle():
-    """The bench's e2e configuration (the wave, groups of 8 prompts), sampled against the
-    oracle."""
+@pytest.mark.parametrize("group", [4, 8])
+def test_host_prefill_wave_vs_oracle(group):
+    """The bench's e2e configuration (the wave in groups of 4 prompts, and of 8), sampled
+    against the oracle: prompts in the first, a middle and the last group."""
     p = I.chat_wave()
-    got = _host_run(p, 8)
+    got = _host_run(p, group)
     compare_units(p, got, [0, 9, 31], [0, 1, 30, 31])
 
 
