@@ -72,6 +72,7 @@ constexpr uint32_t KQ_BYTES = 32768, V_BYTES = 16384;
 struct ChunkedParams {
   PrefillArgs a;
   CUtensorMap tq, tk, tv;  // 2D bf16 maps: (H*128 columns, T rows), 64 x 64 boxes, SW128
+  CUtensorMap to;          // o: (H_v*128 columns, T rows), 64-row x 128-column boxes, no swizzle
 };
 
 struct __align__(8) Smem {
@@ -343,6 +344,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
   // copies and products in flight (meaningful in thread 0, which issues them)
   bool kq_inflight = nchunks > 0 && !p.test_skip_first_copy;
   bool v_inflight = nchunks > 0 && !vz, mma_inflight = false;
+  bool store_pending = false;  // a TMA store of output rows still reading the staging tile
   int c_next = sd.ckpt_begin;
 
   for (int c = 0; c < nchunks && ok; ++c) {
@@ -409,6 +411,12 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
                                   ((cc ^ (r & 7)) << 4)) =
             (int)r < L && !vz ? bf16x8_to_half8(w[pass]) : zero;
       }
+    }
+    // the previous chunk's output store must have read its staging tile (it shares shared
+    // memory with A, written right after this barrier)
+    if (tid == 0 && store_pending) {
+      bulk_wait_read_all();
+      store_pending = false;
     }
     if (!(ok = wait_all(&sm.bar_mma, ph_mma, mma_inflight))) break;
 
@@ -667,14 +675,25 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       }
       if (emit) ++c_next;
       tmem_st_wait();
+      if (L == kC) fence_proxy_async_smem();  // the staged rows go out by TMA
       __syncthreads();
-      // coalesced 16-byte stores of the chunk's output rows
+      if (L == kC) {
+        // a whole chunk lies inside the prompt: one TMA store of the 64 x 128 tile
+        if (tid == 0) {
+          tma_store_2d(&P.to, sO, h * kD, sd.tok_start + t0);
+          bulk_commit();
+          store_pending = true;
+        }
+      } else {
+        // the tail chunk: only its L rows (a whole box would reach the next prompt's rows),
+        // by coalesced 16-byte stores
 #pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int idx = it * kThreads + tid, t = idx >> 4, ch = idx & 15;
-        if (t < L)
-          *reinterpret_cast<uint4*>(og + (size_t)(t0 + t) * v_stride + ch * 8) =
-              *reinterpret_cast<const uint4*>(sO + t * 256 + ch * 16);
+        for (int it = 0; it < 4; ++it) {
+          const int idx = it * kThreads + tid, t = idx >> 4, ch = idx & 15;
+          if (t < L)
+            *reinterpret_cast<uint4*>(og + (size_t)(t0 + t) * v_stride + ch * 8) =
+                *reinterpret_cast<const uint4*>(sO + t * 256 + ch * 16);
+        }
       }
     }
     tc_fence_before();
@@ -701,6 +720,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       if (v_inflight) mbar_wait_bounded(&sm.bar_v, ph_v & 1u, kWaitLimit);
     }
   }
+  if (tid == 0 && store_pending) bulk_wait_all();  // output stores done before the CTA exits
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tbase, TM_COLS);
@@ -719,7 +739,8 @@ int launch_chunked_throughput(const PrefillArgs& a, int64_t total_tokens, void* 
   }
   ChunkedParams P;
   P.a = a;
-  if (!make_qkv_maps(a, total_tokens, kD, &P.tq, &P.tk, &P.tv))
+  if (!make_qkv_maps(a, total_tokens, kD, &P.tq, &P.tk, &P.tv) ||
+      !make_out_map(&P.to, a.o, (uint64_t)a.hv_heads * kD, (uint64_t)total_tokens))
     return (int)cudaErrorInvalidValue;
   chunked_prefill_kernel<<<a.num_units, kThreads, SMEM_BYTES,
                                  static_cast<cudaStream_t>(stream)>>>(P);

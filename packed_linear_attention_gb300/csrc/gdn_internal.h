@@ -150,6 +150,9 @@ int launch_short_units(const PrefillArgs& a, void* stream);
 // q, k (H_k * d columns) and v (H_v * d columns) with total_tokens rows (gdn_tma.cu).
 bool make_qkv_maps(const PrefillArgs& a, int64_t total_tokens, int head_dim, CUtensorMap* tq,
                    CUtensorMap* tk, CUtensorMap* tv);
+// 2D bf16 tensor map over the output o ([rows][cols], row-major) with 64-row x 128-column
+// boxes and no swizzle, for TMA stores of whole chunks of one head's output rows.
+bool make_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows);
 
 // Sequence splitting (gdn_split.cu). fill_states modes besides "copy the caller's state of
 // prompt i" (i >= 0):

@@ -49,6 +49,22 @@ bool make_bf16_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t row
          CUDA_SUCCESS;
 }
 
+bool make_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows) {
+  if (rows == 0) {
+    memset(m, 0, sizeof(CUtensorMap));
+    return true;
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {128, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_qkv_maps(const PrefillArgs& a, int64_t total_tokens, int head_dim, CUtensorMap* tq,
                    CUtensorMap* tk, CUtensorMap* tv) {
   if (total_tokens <= 0) {

@@ -158,6 +158,29 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t
       : "memory");
 }
 
+// One box from shared memory to a tensor in global memory (bulk-group completion). The
+// source must be visible to the async proxy (fence_proxy_async_smem by its writers first).
+__device__ __forceinline__ void tma_store_2d(const void* tmap, const void* src, int32_t x,
+                                             int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(x), "r"(y), "r"(smem_u32(src))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits (in hardware, no polling) until this thread's committed bulk stores have read their
+// shared-memory source, so the source may be overwritten.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until this thread's committed bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Pull one box of a tensor into L2 ahead of its load (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
