@@ -65,13 +65,13 @@ def algorithmic_flops(T, Hk, Hv, d, C=64):
 MEASURED_TRAFFIC = {
     "sources": {
         "packed_linear_attention_gb300/csrc/gdn_chunked.cu":
-            "063c679e6977bd8dd3e3a6a49df8b1937e7ecc7ef9f92521b5a4173e3750a832",
+            "228ea4f4c8743f0f1db3cd595e7ad060aae18b9c071a79bc6bb2c73388aa98a0",
         "packed_linear_attention_gb300/csrc/gdn_chunk_util.cuh":
             "e0236f840d351cdce6c937270bc974f932a44168f7bb01f7583bd2cd4def152d",
         "packed_linear_attention_gb300/csrc/ptx_sm103.cuh":
-            "8d1cb743537c6ed6b8227be46d40fc68426452810e0b9a00659c0e8ba1f86b1f",
+            "7656f71f13ce2d5d3e3fa32de31a5fce86755fc036450c47a26a30d1a01c6b56",
         "packed_linear_attention_gb300/csrc/gdn_tma.cu":
-            "a436f19726f8b42f0f87a2c8198857b0854bf15e7d0b549380f7dd32d6fd4129",
+            "0336c41ea051cad488f5d43c034eb75bee8fb8e3fc662d50a87f672d267ebdcb",
     },
     "read_bytes": 546.0e6,
     "write_bytes": 357.0e6,

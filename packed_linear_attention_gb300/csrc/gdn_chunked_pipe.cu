@@ -92,6 +92,7 @@ enum : int { B_KQ0, B_KQ1, B_V, B_M1, B_M2, B_READY0, B_READY1, B_D, B_S, B_O, B
 struct ChunkedParams {
   PrefillArgs a;
   CUtensorMap tq, tk, tv;  // 2D bf16 maps: (H*128 columns, T rows), 64 x 64 boxes, SW128
+  CUtensorMap to;          // o: (H_v*128 columns, T rows), 64-row x 128-column boxes, no swizzle
 };
 
 struct __align__(8) Smem {
@@ -528,6 +529,7 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
     float gnext[4] = {0.f, 0.f, 0.f, 0.f};  // its raw gate loads of the next chunk to stage
     if (warp == kGateWarp && nchunks > 0) fetch_gates(ag, bg, p.hv_heads, 0, sd.len, lane, gnext);
     bool ok = true, lead_fail = false;
+    bool store_pending = false;  // (leader) a TMA store of output rows still reading sO
 
     // Gate factors of chunk cc into factor buffer cc & 1 and its total decay into
     // sm.gamma[cc & 1] (gate warp only; published by the next stage_chunk(cc)).
@@ -636,6 +638,11 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
       const Factors f(reinterpret_cast<float*>(smem + OFF_VEC + b * 2048));
 
       // ---- (C1) D^T = U^T - S16 W^T is ready: D^T and D'^T = D^T diag(dec) -> smem (fp16) ---
+      // (the previous chunk's output store must have read sO, which D^T overwrites)
+      if (leader && store_pending) {
+        bulk_wait_read_all();
+        store_pending = false;
+      }
       if (!(ok = group_wait(sm, B_D, c & 1, kBarChain, leader, lead_fail))) break;
       {
         uint32_t r[32];
@@ -766,15 +773,26 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
         }
         tmem_st_wait();
       }
+      if (L == kC) fence_proxy_async_smem();  // the staged rows go out by TMA
       tc_fence_before();
       named_sync(kBarChain, kGroup);
-      // coalesced 16-byte stores of the chunk's output rows
+      if (L == kC) {
+        // a whole chunk lies inside the prompt: one TMA store of the 64 x 128 tile
+        if (leader) {
+          tma_store_2d(&P.to, sO, h * kD, sd.tok_start + t0);
+          bulk_commit();
+          store_pending = true;
+        }
+      } else {
+        // the tail chunk: only its L rows (a whole box would reach the next prompt's rows),
+        // by coalesced 16-byte stores
 #pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int idx = it * kGroup + ctid, t = idx >> 4, ch = idx & 15;
-        if (t < L)
-          *reinterpret_cast<uint4*>(og + (size_t)(t0 + t) * v_stride + ch * 8) =
-              *reinterpret_cast<const uint4*>(sO + t * 256 + ch * 16);
+        for (int it = 0; it < 4; ++it) {
+          const int idx = it * kGroup + ctid, t = idx >> 4, ch = idx & 15;
+          if (t < L)
+            *reinterpret_cast<uint4*>(og + (size_t)(t0 + t) * v_stride + ch * 8) =
+                *reinterpret_cast<const uint4*>(sO + t * 256 + ch * 16);
+        }
       }
 
       // ---- (C6) stage chunk c+2 (copied into buffer b since C3) ------------------------------
@@ -796,6 +814,7 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
     if (leader) {
       mma_commit(&sm.bar[B_FLUSH_C]);
       mbar_wait_bounded(&sm.bar[B_FLUSH_C], 0, kWaitLimit);
+      if (store_pending) bulk_wait_all();  // output stores done before the CTA exits
     }
 
     if (ok && sd.len == 0) {
@@ -835,7 +854,8 @@ int launch_chunked_pipelined(const PrefillArgs& a, int64_t total_tokens, void* s
   }
   ChunkedParams P;
   P.a = a;
-  if (!make_qkv_maps(a, total_tokens, kD, &P.tq, &P.tk, &P.tv))
+  if (!make_qkv_maps(a, total_tokens, kD, &P.tq, &P.tk, &P.tv) ||
+      !make_out_map(&P.to, a.o, (uint64_t)a.hv_heads * kD, (uint64_t)total_tokens))
     return (int)cudaErrorInvalidValue;
   chunked_pipe_kernel<<<a.num_units, kThreads, SMEM_BYTES,
                                  static_cast<cudaStream_t>(stream)>>>(P);
