@@ -17,7 +17,8 @@ namespace chunk {
 constexpr int kC = 64;          // tokens per chunk
 constexpr int kD = 128;         // head dim
 constexpr int kLd = 68;         // fp32 64x64 matrix row stride (conflict-free float4 rows)
-constexpr int kLdX = 36;        // row stride of the 32 x 32 merge scratch
+constexpr int kLdX = 40;        // row stride of the 32 x 32 merge scratch (8 mod 32: its
+                                // tf32 B-fragment loads fall on distinct banks)
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr int kStatusTimeout = 5;  // GDN_ERR_DEVICE_TIMEOUT
 constexpr float kLog2e = 1.4426950408889634f;

@@ -59,7 +59,7 @@ constexpr uint32_t OFF_V = 32768;      // V: 2 regions x 8 KB
 constexpr uint32_t OFF_P = 49152;      // P: 64 x 64 fp16
 constexpr uint32_t OFF_A = 57344;      // A fp32 [64][68] -> T1 (first 8 KB) -> D' -> o staging
 constexpr uint32_t OFF_WD = 75776;     // T fp32 [64][68] -> W^T -> D
-constexpr uint32_t OFF_XS = OFF_WD + 17408;  // inverse scratch: 32 x 36 fp32
+constexpr uint32_t OFF_XS = OFF_WD + 17408;  // inverse scratch: 32 x 40 fp32
 constexpr uint32_t OFF_VEC = OFF_XS + 5120;  // per-token gate factors: 8 x 64 fp32
 constexpr uint32_t OFF_T2 = OFF_VEC + 2048;  // T2 (fp16 64 x 64), a region of its own
 static_assert(OFF_T2 % 1024 == 0, "shared-memory map");
@@ -88,7 +88,9 @@ constexpr int kGateWarp = 2;
 // Waits (every thread, bounded) for the pending phase of an mbarrier, with one answer for
 // the whole block (false on a timeout). A phase that a thread saw complete advances its
 // `phase` and clears its `pending`; after a timeout both still name the pending phase, for
-// the cleanup.
+// the cleanup. (Thread 0 polling alone, the other warps waiting at the block barrier, was
+// measured slower: the barrier's wake-up after the phase completes costs more than the
+// polls take from the other CTA on the SM.)
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t& phase, bool& pending) {
   const bool ok = mbar_wait_bounded(bar, phase & 1u, kWaitLimit);
   if (ok) {
@@ -203,8 +205,10 @@ __device__ void invert_merge(const float* A, float* T, float* X, uint8_t* T1, ui
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     tile_mm(d, A + 32 * kLd, kLd, r0, T, kLd, n0, nt >= 2 ? 16 : 0, 32, gid, tig);
     // while the warp MMAs run: every block of T1/T2 but T[32:64, 0:32], from T (16
-    // columns of one row per thread)
-    const int i = tid >> 2, jb = (tid & 3) * 16;
+    // columns of one row per thread; a warp takes 8 rows, and the 8 lanes of each quarter
+    // warp 8 consecutive rows at the same columns, so that their float4 reads of T fall on
+    // distinct banks and those of the column factors are broadcasts)
+    const int i = 8 * warp + (lane & 7), jb = (lane >> 3) * 16;
     if (i < 32 || jb >= 32) {
 #pragma unroll
       for (int h8 = 0; h8 < 16; h8 += 8) {

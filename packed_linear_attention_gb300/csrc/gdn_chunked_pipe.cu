@@ -71,7 +71,7 @@ static_assert(OFF_D == 131072, "shared-memory map");
 constexpr uint32_t OFF_DP = 147456;     // D'^T (fp16)
 constexpr uint32_t OFF_A = 163840;      // A fp32 [64][68]
 constexpr uint32_t OFF_T = OFF_A + 17408;   // T fp32 [64][68]
-constexpr uint32_t OFF_XS = OFF_T + 17408;  // inverse scratch: 32 x 36 fp32
+constexpr uint32_t OFF_XS = OFF_T + 17408;  // inverse scratch: 32 x 40 fp32
 constexpr uint32_t OFF_VEC = OFF_XS + 5120;  // 2 buffers x per-token factors (8 x 64 fp32)
 constexpr uint32_t OFF_T12 = OFF_VEC + 4096;  // T1 | T2 (fp16 64 x 64); blocks above the diagonal stay 0
 constexpr uint32_t SMEM_USED = OFF_T12 + 16384;
