@@ -204,33 +204,35 @@ __device__ void invert_merge(const float* A, float* T, float* X, uint8_t* T1, ui
   {
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     tile_mm(d, A + 32 * kLd, kLd, r0, T, kLd, n0, nt >= 2 ? 16 : 0, 32, gid, tig);
-    // while the warp MMAs run: every block of T1/T2 but T[32:64, 0:32], from T (16
-    // columns of one row per thread; a warp takes 8 rows, and the 8 lanes of each quarter
-    // warp 8 consecutive rows at the same columns, so that their float4 reads of T fall on
-    // distinct banks and those of the column factors are broadcasts)
-    const int i = 8 * warp + (lane & 7), jb = (lane >> 3) * 16;
-    if (i < 32 || jb >= 32) {
+    // while the warp MMAs run: the two diagonal 32 x 32 blocks of T1/T2, from T, and the
+    // zero block above them. A thread takes 8 columns of one row of a diagonal block (warps
+    // 0-3 the first, 4-7 the second) and one 16-byte chunk of zeros; the 8 lanes of each
+    // quarter warp take 8 consecutive rows at the same columns, so that their float4 reads
+    // of T fall on distinct banks and those of the column factors are broadcasts.
+    {
+      const int bk = warp >> 2, i = 32 * bk + 8 * (warp & 3) + (lane & 7);
+      const int j0 = 32 * bk + 8 * (lane >> 3);
+      float x1[8], x2[8];
 #pragma unroll
-      for (int h8 = 0; h8 < 16; h8 += 8) {
-        float x1[8], x2[8];
+      for (int q4 = 0; q4 < 8; q4 += 4) {
+        const int j = j0 + q4;
+        const float4 tv = *reinterpret_cast<const float4*>(T + i * kLd + j);
+        const float4 gv = *reinterpret_cast<const float4*>(c1 + j);
+        const float4 bv = *reinterpret_cast<const float4*>(c2 + j);
+        const float t4[4] = {tv.x, tv.y, tv.z, tv.w}, g4[4] = {gv.x, gv.y, gv.z, gv.w},
+                    b4[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-        for (int q4 = 0; q4 < 8; q4 += 4) {
-          const int j = jb + h8 + q4;
-          const float4 tv = *reinterpret_cast<const float4*>(T + i * kLd + j);
-          const float4 gv = *reinterpret_cast<const float4*>(c1 + j);
-          const float4 bv = *reinterpret_cast<const float4*>(c2 + j);
-          const float t4[4] = {tv.x, tv.y, tv.z, tv.w}, g4[4] = {gv.x, gv.y, gv.z, gv.w},
-                      b4[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-          for (int f = 0; f < 4; ++f) {
-            const float tij = j + f <= i ? t4[f] : 0.f;
-            x1[q4 + f] = tij * g4[f];
-            x2[q4 + f] = tij * b4[f];
-          }
+        for (int f = 0; f < 4; ++f) {
+          const float tij = j + f <= i ? t4[f] : 0.f;  // zero above the diagonal
+          x1[q4 + f] = tij * g4[f];
+          x2[q4 + f] = tij * b4[f];
         }
-        st_chunk(T1, i, jb + h8, 64, x1);
-        st_chunk(T2, i, jb + h8, 64, x2);
       }
+      st_chunk(T1, i, j0, 64, x1);
+      st_chunk(T2, i, j0, 64, x2);
+      // T1 (warps 0-3) or T2 (warps 4-7), rows 0-31, columns 32-63
+      *reinterpret_cast<uint4*>((bk ? T2 : T1) + ptx::sw128_offset(i - 32 * bk, j0 + 32 - 32 * bk, 64)) =
+          make_uint4(0u, 0u, 0u, 0u);
     }
     tile_store(X, kLdX, r0, n0, d, 1.f, gid, tig);
   }
