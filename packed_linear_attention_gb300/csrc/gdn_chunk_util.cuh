@@ -209,6 +209,45 @@ __device__ __forceinline__ void convert_kq(uint8_t* sKQ, const Factors& f, int L
   }
 }
 
+// Column j of the inverse of the unit lower-triangular 16 x 16 block I + A[o:o+16, o:o+16]
+// (A strictly lower, fp32, row stride kLd) into x: x_i = delta_ij - sum_{k<i} A_ik x_k, by
+// forward substitution. Every x_i is the same chain of fused multiply-adds over k in
+// ascending order in both forms below, so they give the same bits:
+//  * diag_block_column (row by row) reads row i of the block as float4s that every lane
+//    handling the block shares (broadcasts): 36 loads instead of one per term;
+//  * diag_block_column_rl (column by column: x_k, once final, is taken out of every later
+//    row) reads one element per term and holds fewer registers, for the 16-warp schedule,
+//    whose register budget the row form overflows.
+__device__ __forceinline__ void diag_block_column(const float* A, int o, int j,
+                                                  float (&x)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float acc = i == j ? 1.f : 0.f;
+    const float* ar = A + (o + i) * kLd + o;
+#pragma unroll
+    for (int k4 = 0; k4 < i; k4 += 4) {
+      const float4 a = *reinterpret_cast<const float4*>(ar + k4);
+      const float a4[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int f = 0; f < 4; ++f)
+        if (k4 + f < i) acc = __fmaf_rn(-a4[f], x[k4 + f], acc);
+    }
+    x[i] = acc;
+  }
+}
+
+__device__ __forceinline__ void diag_block_column_rl(const float* A, int o, int j,
+                                                     float (&x)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) x[i] = i == j ? 1.f : 0.f;
+#pragma unroll
+  for (int k = 0; k < 15; ++k) {
+    const float xk = x[k];
+#pragma unroll
+    for (int i = k + 1; i < 16; ++i) x[i] = __fmaf_rn(-A[(o + i) * kLd + o + k], xk, x[i]);
+  }
+}
+
 // One 16 x 8 output tile D += sum_k Ablk[r0.., k] * Bblk[k.., n0..] over k in [k_lo, k_hi)
 // (multiples of 8, at most 32 wide) on one warp, tf32 warp MMAs. Both matrices fp32 with
 // row strides lda/ldb. Each 8-wide k step goes into a zeroed tile of its own and the partial

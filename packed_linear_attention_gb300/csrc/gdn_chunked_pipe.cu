@@ -174,7 +174,7 @@ __device__ __forceinline__ void commit(Smem& sm, int i) {
 
 
 // (I + A)^-1 for a 64 x 64 strictly-lower A (fp32, row stride kLd) into T (same stride):
-//  1. (invert_diag_blocks) the four 16 x 16 diagonal blocks by right-looking forward
+//  1. (invert_diag_blocks) the four 16 x 16 diagonal blocks by forward
 //     substitution in fp32 (two blocks per warp, one column per lane);
 //  2. (invert_merge) recursive doubling: for L = [[L11, 0], [L21, L22]], L^-1 has
 //     off-diagonal block -L22^-1 L21 L11^-1; first for the 16 x 16 pairs, then for the two
@@ -193,14 +193,7 @@ __device__ __forceinline__ void invert_diag_blocks(const float* A, float* T, uin
                                                    const float* c2, int pair, int lane) {
   const int o = 16 * (2 * pair + (lane >> 4)), j = lane & 15;
   float x[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) x[i] = i == j ? 1.f : 0.f;
-#pragma unroll
-  for (int k = 0; k < 15; ++k) {
-    const float xk = x[k];
-#pragma unroll
-    for (int i = k + 1; i < 16; ++i) x[i] -= A[(o + i) * kLd + o + k] * xk;
-  }
+  diag_block_column_rl(A, o, j, x);
   const float f1 = c1[o + j], f2 = c2[o + j];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
