@@ -209,6 +209,84 @@ __device__ __forceinline__ void convert_kq(uint8_t* sKQ, const Factors& f, int L
   }
 }
 
+// Chunks whose total log2-decay is at least this take the factored form of the A/P
+// epilogue (ap_row): their column factors 2^{-Gp_j} = 2^{-G_j} / |k_j| stay below 2^110,
+// since 1/|k_j| <= 1/sqrt(kL2NormEps) < 2^10.
+constexpr float kFactoredMinLog2Decay = -100.f;
+
+// Column factor of the factored A/P epilogue for token j: 2^{-Gp_j} = e^{-G_j} / |k_j| (0
+// for padded tokens, whose Gp is +inf). Written by the warp that folds the norms into Gp.
+__device__ __forceinline__ float col_factor(float gp) { return ptx::ex2(-gp); }
+
+// One thread's 32 columns j0..j0+31 of row `row` of the first product [K;Q]K^T (r: its fp32
+// accumulators) scaled into
+//   A (rows 0-63):   A_ij = beta_i e^{G_i - G_j} (k_i . k_j) / (|k_i| |k_j|)  for j < i, else 0
+//                    (fp32, row stride kLd), or
+//   P (rows 64-127): P_tj = scale e^{G_t - G_j} (q_t . k_j) / (|q_t| |k_j|)  for j <= t, else 0
+//                    (fp16 128B-swizzled tile).
+// The scale factor of an entry is 2^{x_i - Gp_j}, with x_i the row's exponent (G_i plus the
+// log2 of its beta, or scale, and inverse norm). With `factored` (the chunk's total log2-decay
+// is at least kFactoredMinLog2Decay) it is split as 2^{x_i} 2^{-Gp_j}, and an entry costs two
+// multiplies with the column factors cf (col_factor) read from shared memory. Both factors
+// are finite; below the diagonal their product is the entry's factor (at most 1 before the
+// norms), and above it, where the product may overflow to inf, the entry is masked to 0
+// (no NaN: the first product is finite). A row factor below the normal range only scales
+// entries far below the fp16 rounding of T. Otherwise every entry takes its own ex2 of the
+// difference, which is never above 0 below the diagonal. Both schedules call this one
+// function, so that A and P agree bit for bit between them.
+template <bool kFactored>
+__device__ __forceinline__ void ap_row_form(const uint32_t (&r)[32], uint32_t row, int j0,
+                                            const Factors& f, const float* cf, float scale,
+                                            float* sA, uint8_t* sP) {
+  const float* w_src = kFactored ? cf : f.Gp;  // column factors or column exponents
+  if (row < 64) {
+    const int i = row;
+    const float xi = f.G[i] + __log2f(f.B[i] * f.Rk[i]);
+    const float ri = kFactored ? ptx::ex2(xi) : 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      const float4 w = *reinterpret_cast<const float4*>(w_src + j0 + e);
+      const float w4[4] = {w.x, w.y, w.z, w.w};
+      float4 v;
+      float* vv = reinterpret_cast<float*>(&v);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float a = __uint_as_float(r[e + q]);
+        const float x = kFactored ? (a * ri) * w4[q] : a * ptx::ex2(xi - w4[q]);
+        vv[q] = j0 + e + q < i ? x : 0.f;
+      }
+      *reinterpret_cast<float4*>(sA + i * kLd + j0 + e) = v;
+    }
+  } else {
+    const int t = row - 64;
+    const float xt = f.G[t] + __log2f(scale * f.Rq[t]);
+    const float rt = kFactored ? ptx::ex2(xt) : 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; e += 8) {
+      const float4 wa = *reinterpret_cast<const float4*>(w_src + j0 + e);
+      const float4 wb = *reinterpret_cast<const float4*>(w_src + j0 + e + 4);
+      const float w8[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+      float x[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float a = __uint_as_float(r[e + q]);
+        const float y = kFactored ? (a * rt) * w8[q] : a * ptx::ex2(xt - w8[q]);
+        x[q] = j0 + e + q <= t ? y : 0.f;
+      }
+      st_chunk(sP, t, j0 + e, 64, x);
+    }
+  }
+}
+
+__device__ __forceinline__ void ap_row(const uint32_t (&r)[32], uint32_t row, int j0,
+                                       const Factors& f, const float* cf, float scale,
+                                       bool factored, float* sA, uint8_t* sP) {
+  if (factored)
+    ap_row_form<true>(r, row, j0, f, cf, scale, sA, sP);
+  else
+    ap_row_form<false>(r, row, j0, f, cf, scale, sA, sP);
+}
+
 // Column j of the inverse of the unit lower-triangular 16 x 16 block I + A[o:o+16, o:o+16]
 // (A strictly lower, fp32, row stride kLd) into x: x_i = delta_ij - sum_{k<i} A_ik x_k, by
 // forward substitution. Every x_i is the same chain of fused multiply-adds over k in

@@ -387,6 +387,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
         const int i = lane + 32 * hh;
         const float rk = sRk[i], rq = sRq[i];
         sGp[i] = sG[i] - __log2f(rk);  // +inf for padded tokens: their column terms vanish
+        sXs[i] = col_factor(sGp[i]);    // (the merge scratch is idle until the inverse)
         sBG[i] *= rk;
         sDec[i] *= rk;
         sGq[i] *= rq;
@@ -432,40 +433,8 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       uint32_t r[32];
       tmem_ld32(t_lane + TM_R0 + 32 * half, r);
       tmem_ld_wait();
-      const int j0 = 32 * half;
-      if (row < 64) {
-        const int i = row;
-        const float gi = sG[i] + __log2f(sB[i] * sRk[i]);  // row factor in the exponent
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 gj = *reinterpret_cast<const float4*>(sGp + j0 + e);
-          const float g4[4] = {gj.x, gj.y, gj.z, gj.w};
-          float4 v;
-          float* vv = reinterpret_cast<float*>(&v);
-#pragma unroll
-          for (int f = 0; f < 4; ++f) {
-            const float x = __uint_as_float(r[e + f]) * ex2(gi - g4[f]);
-            vv[f] = j0 + e + f < i ? x : 0.f;
-          }
-          *reinterpret_cast<float4*>(sA + i * kLd + j0 + e) = v;
-        }
-      } else {
-        const int t = row - 64;
-        const float gt = sG[t] + __log2f(scale * sRq[t]);  // row factor in the exponent
-#pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          const float4 ga = *reinterpret_cast<const float4*>(sGp + j0 + e);
-          const float4 gb = *reinterpret_cast<const float4*>(sGp + j0 + e + 4);
-          const float g8[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-          float x[8];
-#pragma unroll
-          for (int f = 0; f < 8; ++f) {
-            const float y = __uint_as_float(r[e + f]) * ex2(gt - g8[f]);
-            x[f] = j0 + e + f <= t ? y : 0.f;
-          }
-          st_chunk(sP, t, j0 + e, 64, x);
-        }
-      }
+      ap_row(r, row, 32 * half, Factors(sG), sXs, scale, sG[63] >= kFactoredMinLog2Decay, sA,
+             sP);
     }
     tc_fence_before();
 

@@ -377,6 +377,7 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
           const int i = lane + 32 * hh;
           const float rk = f.Rk[i], rq = f.Rq[i];
           f.Gp[i] = f.G[i] - __log2f(rk);  // +inf for padded tokens: their column terms vanish
+          sXs[i] = col_factor(f.Gp[i]);   // (the merge scratch is idle until the inverse)
           f.BG[i] *= rk;
           f.Dec[i] *= rk;
           f.Gq[i] *= rq;
@@ -397,40 +398,7 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
         uint32_t r[32];
         tmem_ld32(t_lane + TM_M + 32 * half, r);
         tmem_ld_wait();
-        const int j0 = 32 * half;
-        if (row < 64) {
-          const int i = row;
-          const float gi = f.G[i] + __log2f(f.B[i] * f.Rk[i]);  // row factor in the exponent
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 gj = *reinterpret_cast<const float4*>(f.Gp + j0 + e);
-            const float g4[4] = {gj.x, gj.y, gj.z, gj.w};
-            float4 v;
-            float* vv = reinterpret_cast<float*>(&v);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float x = __uint_as_float(r[e + q]) * ex2(gi - g4[q]);
-              vv[q] = j0 + e + q < i ? x : 0.f;
-            }
-            *reinterpret_cast<float4*>(sA + i * kLd + j0 + e) = v;
-          }
-        } else {
-          const int t = row - 64;
-          const float gt = f.G[t] + __log2f(scale * f.Rq[t]);  // row factor in the exponent
-#pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            const float4 ga = *reinterpret_cast<const float4*>(f.Gp + j0 + e);
-            const float4 gb = *reinterpret_cast<const float4*>(f.Gp + j0 + e + 4);
-            const float g8[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-            float x[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float y = __uint_as_float(r[e + q]) * ex2(gt - g8[q]);
-              x[q] = j0 + e + q <= t ? y : 0.f;
-            }
-            st_chunk(sP, t, j0 + e, 64, x);
-          }
-        }
+        ap_row(r, row, 32 * half, f, sXs, scale, f.G[63] >= kFactoredMinLog2Decay, sA, sP);
       }
       tc_fence_before();
 
