@@ -236,6 +236,29 @@ def test_chunked_schedules_agree_bitwise(case, ragged):
     _assert_same(run(p, gdn.KERNEL_CHUNKED_PIPELINED), run(p, gdn.KERNEL_CHUNKED_THROUGHPUT))
 
 
+def test_decay_factor_forms_straddle_threshold():
+    """The A/P epilogue splits each entry's decay factor into a row and a column factor in
+    chunks whose total log2-decay is at least -100 and takes one ex2 per entry in stronger
+    chunks. A pack whose chunks fall on both sides of that bound (checked here from the
+    gates) matches the oracle under both schedules, which agree bit for bit."""
+    torch_cuda()
+    lengths = [256, 200, 320, 129]
+    p = I.make_pack(lengths, num_k_heads=2, num_v_heads=4, head_dim=128, io_dtype="bf16",
+                    seed=41, init_std=0.02, ckpt_lists=[[128], [], [64, 320], [129]],
+                    decay_scale=1.35)
+    totals = []
+    for n in range(len(lengths)):
+        a = p.a[p.cu_seqlens[n]:p.cu_seqlens[n + 1]].astype(np.float64)
+        for c0 in range(0, lengths[n], 64):
+            totals.extend(a[c0:c0 + 64].sum(axis=0) / np.log(2.0))
+    totals = np.array(totals)
+    assert (totals >= -100).any() and (totals < -100).any()
+    pipe = run(p, gdn.KERNEL_CHUNKED_PIPELINED)
+    thr = run(p, gdn.KERNEL_CHUNKED_THROUGHPUT)
+    _assert_same(pipe, thr)
+    compare_units(p, thr, list(range(len(lengths))), list(range(4)), per_item=False)
+
+
 def test_automatic_choice_equals_forced_schedules(wave):
     """The automatic result on the wave (throughput schedule) equals either forced
     schedule bit for bit."""
