@@ -65,9 +65,9 @@ def algorithmic_flops(T, Hk, Hv, d, C=64):
 MEASURED_TRAFFIC = {
     "sources": {
         "packed_linear_attention_gb300/csrc/gdn_chunked.cu":
-            "228ea4f4c8743f0f1db3cd595e7ad060aae18b9c071a79bc6bb2c73388aa98a0",
+            "617fcc340d2cace43f6a164452edf5eb1569a5ce419ee7af548ad0e5791ac66b",
         "packed_linear_attention_gb300/csrc/gdn_chunk_util.cuh":
-            "e0236f840d351cdce6c937270bc974f932a44168f7bb01f7583bd2cd4def152d",
+            "31ea72c253f10039cbce7a7b89024ca5afc4fd8a37a8938cb481b82c221d4590",
         "packed_linear_attention_gb300/csrc/ptx_sm103.cuh":
             "7656f71f13ce2d5d3e3fa32de31a5fce86755fc036450c47a26a30d1a01c6b56",
         "packed_linear_attention_gb300/csrc/gdn_tma.cu":
