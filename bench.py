@@ -100,23 +100,27 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every `period_ms` while running; each
+    sample keeps the host time at which it arrived, so that a summary can be restricted to
+    a window (the loaded part of the run)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 20):
         self.gpu = gpu_index
+        self.period_ms = period_ms
         self.proc = None
-        self.lines: list[str] = []
+        self.lines: list[tuple[float, str]] = []
         self._t = None
+        self.window = None  # (t0, t1) host monotonic times, set by the caller
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
@@ -126,7 +130,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def live(self) -> bool:
+        """True once a sample has arrived (or when nvidia-smi could not be started)."""
+        return self.proc is None or bool(self.lines)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -141,9 +149,11 @@ class ClockSampler:
     def summary(self):
         if not self.lines:
             return None
+        lines = [ln for t, ln in self.lines
+                 if self.window is None or self.window[0] <= t <= self.window[1]]
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -158,7 +168,9 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window": "the timed steps and an untimed tail of the same steps (>= 0.25 s), "
+                          f"sampled every {self.period_ms} ms"}
 
 
 def dist_env():
@@ -277,15 +289,33 @@ def run_gpu(args):
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
     with ClockSampler(dev.index) as clocks:
+        # the same steps, untimed, until nvidia-smi delivers samples (at most 5 s)
+        t_wait = time.monotonic()
+        while not clocks.live() and time.monotonic() - t_wait < 5.0:
+            for _ in range(16):
+                flush.zero_()
+                step()
+            torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        t_on = time.monotonic()
         for i in range(args.steps):
             flush.zero_()
             starts[i].record(stream)
             step()
             ends[i].record(stream)
         torch.cuda.synchronize()
+        # an untimed tail of the same steps, so that a timed region shorter than the sampling
+        # period still has samples taken under its load
+        t_off = time.monotonic()
+        while time.monotonic() - t_off < 0.25:
+            for _ in range(16):
+                flush.zero_()
+                step()
+            torch.cuda.synchronize()
+        clocks.window = (t_on, time.monotonic())
+    assert gdn.gdn_read_device_status(buf.workspace) == 0
     barrier(world)
     per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_local = sum(per) / len(per)
