@@ -247,14 +247,25 @@ __device__ __forceinline__ void ap_row_form(const uint32_t (&r)[32], uint32_t ro
     for (int e = 0; e < 32; e += 4) {
       const float4 w = *reinterpret_cast<const float4*>(w_src + j0 + e);
       const float w4[4] = {w.x, w.y, w.z, w.w};
+      float x4[4];
+      if (kFactored) {  // (a ri) w per entry, two entries per packed multiply
+#pragma unroll
+        for (int q = 0; q < 4; q += 2) {
+          const float2 t = ptx::mul2(
+              make_float2(__uint_as_float(r[e + q]), __uint_as_float(r[e + q + 1])),
+              make_float2(ri, ri));
+          const float2 y = ptx::mul2(t, make_float2(w4[q], w4[q + 1]));
+          x4[q] = y.x;
+          x4[q + 1] = y.y;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x4[q] = __uint_as_float(r[e + q]) * ptx::ex2(xi - w4[q]);
+      }
       float4 v;
       float* vv = reinterpret_cast<float*>(&v);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float a = __uint_as_float(r[e + q]);
-        const float x = kFactored ? (a * ri) * w4[q] : a * ptx::ex2(xi - w4[q]);
-        vv[q] = j0 + e + q < i ? x : 0.f;
-      }
+      for (int q = 0; q < 4; ++q) vv[q] = j0 + e + q < i ? x4[q] : 0.f;
       *reinterpret_cast<float4*>(sA + i * kLd + j0 + e) = v;
     }
   } else {
@@ -267,12 +278,23 @@ __device__ __forceinline__ void ap_row_form(const uint32_t (&r)[32], uint32_t ro
       const float4 wb = *reinterpret_cast<const float4*>(w_src + j0 + e + 4);
       const float w8[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
       float x[8];
+      float y8[8];
+      if (kFactored) {  // (a rt) w per entry, two entries per packed multiply
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float a = __uint_as_float(r[e + q]);
-        const float y = kFactored ? (a * rt) * w8[q] : a * ptx::ex2(xt - w8[q]);
-        x[q] = j0 + e + q <= t ? y : 0.f;
+        for (int q = 0; q < 8; q += 2) {
+          const float2 u = ptx::mul2(
+              make_float2(__uint_as_float(r[e + q]), __uint_as_float(r[e + q + 1])),
+              make_float2(rt, rt));
+          const float2 y = ptx::mul2(u, make_float2(w8[q], w8[q + 1]));
+          y8[q] = y.x;
+          y8[q + 1] = y.y;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) y8[q] = __uint_as_float(r[e + q]) * ptx::ex2(xt - w8[q]);
       }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) x[q] = j0 + e + q <= t ? y8[q] : 0.f;
       st_chunk(sP, t, j0 + e, 64, x);
     }
   }
@@ -371,9 +393,10 @@ __device__ __forceinline__ void tile_store_t12(uint8_t* T1, uint8_t* T2, int r0,
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     const uint32_t off = ptx::sw128_offset(r0 + gid + 8 * hh, col, 64);
-    const float x0 = -d[2 * hh], x1 = -d[2 * hh + 1];
-    *reinterpret_cast<uint32_t*>(T1 + off) = pack_half2(x0 * g0, x1 * g1);
-    *reinterpret_cast<uint32_t*>(T2 + off) = pack_half2(x0 * b0, x1 * b1);
+    const float2 x = make_float2(-d[2 * hh], -d[2 * hh + 1]);
+    const float2 y1 = ptx::mul2(x, make_float2(g0, g1)), y2 = ptx::mul2(x, make_float2(b0, b1));
+    *reinterpret_cast<uint32_t*>(T1 + off) = pack_half2(y1.x, y1.y);
+    *reinterpret_cast<uint32_t*>(T2 + off) = pack_half2(y2.x, y2.y);
   }
 }
 

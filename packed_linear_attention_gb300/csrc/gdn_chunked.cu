@@ -215,10 +215,15 @@ __device__ void invert_merge(const float* A, float* T, float* X, uint8_t* T1, ui
         const float t4[4] = {tv.x, tv.y, tv.z, tv.w}, g4[4] = {gv.x, gv.y, gv.z, gv.w},
                     b4[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-        for (int f = 0; f < 4; ++f) {
-          const float tij = j + f <= i ? t4[f] : 0.f;  // zero above the diagonal
-          x1[q4 + f] = tij * g4[f];
-          x2[q4 + f] = tij * b4[f];
+        for (int f = 0; f < 4; f += 2) {
+          const float2 tij = make_float2(j + f <= i ? t4[f] : 0.f,  // zero above the diagonal
+                                         j + f + 1 <= i ? t4[f + 1] : 0.f);
+          const float2 y1 = mul2(tij, make_float2(g4[f], g4[f + 1]));
+          const float2 y2 = mul2(tij, make_float2(b4[f], b4[f + 1]));
+          x1[q4 + f] = y1.x;
+          x1[q4 + f + 1] = y1.y;
+          x2[q4 + f] = y2.x;
+          x2[q4 + f + 1] = y2.y;
         }
       }
       st_chunk(T1, i, j0, 64, x1);
@@ -533,9 +538,12 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
         const float d8[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
         float x[8], y[8];
 #pragma unroll
-        for (int f = 0; f < 8; ++f) {
+        for (int f = 0; f < 8; f += 2) {
           x[f] = __uint_as_float(r[e + f]);
-          y[f] = x[f] * d8[f];
+          x[f + 1] = __uint_as_float(r[e + f + 1]);
+          const float2 t = mul2(make_float2(x[f], x[f + 1]), make_float2(d8[f], d8[f + 1]));
+          y[f] = t.x;
+          y[f + 1] = t.y;
         }
         st_chunk(sWD, row, 32 * half + e, 128, x);
         st_chunk(sDp, row, 32 * half + e, 128, y);
@@ -633,9 +641,16 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
         } else {
           uint32_t lo[16], hi[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            lo[e] = __float_as_uint(__uint_as_float(s32[e]) * nd);
-            hi[e] = __float_as_uint(__uint_as_float(s32[16 + e]) * nd);
+          for (int e = 0; e < 16; e += 2) {
+            const float2 a = mul2(make_float2(__uint_as_float(s32[e]), __uint_as_float(s32[e + 1])),
+                                  make_float2(nd, nd));
+            const float2 b = mul2(
+                make_float2(__uint_as_float(s32[16 + e]), __uint_as_float(s32[17 + e])),
+                make_float2(nd, nd));
+            lo[e] = __float_as_uint(a.x);
+            lo[e + 1] = __float_as_uint(a.y);
+            hi[e] = __float_as_uint(b.x);
+            hi[e + 1] = __float_as_uint(b.y);
           }
           tmem_st16(t_lane + TM_S32 + 64 * half + c0, lo);
           tmem_st16(t_lane + TM_S32 + 64 * half + c0 + 16, hi);

@@ -200,6 +200,19 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// ---- packed fp32 pairs ----------------------------------------------------------------------
+
+// (a.x * b.x, a.y * b.y) in one instruction (mul.rn.f32x2): each lane is the IEEE
+// round-to-nearest product, bit for bit what two scalar multiplies give.
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n .reg .b64 pa, pb, pc;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %5};\n"
+      " mul.rn.f32x2 pc, pa, pb;\n mov.b64 {%0, %1}, pc;\n}\n"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
 // ---- warp-level tf32 MMA (m16n8k8), used for small fp32 block products -----------------
 
 __device__ __forceinline__ uint32_t to_tf32(float x) {
