@@ -412,7 +412,24 @@ def run_until_ckpt_d2h(torch, gdn, h, buf, stream, flush, steps=10):
         gdn.gdn_checkpoint_copy_wait(h)
         tot += time.perf_counter() - t0
     us = tot / steps * 1e6
-    return {"us": us, "ckpt_bytes": nbytes, "timing": "host clock, launch to copy completion"}
+    # the same with the copies started per group of prompts as their checkpoints are stored
+    for _ in range(3):
+        gdn.prefill_snapshot(h, buf, 0, stream)
+        gdn.gdn_checkpoint_copy_wait(h)
+    tot = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        gdn.prefill_snapshot(h, buf, 0, stream)
+        gdn.gdn_checkpoint_copy_wait(h)
+        tot += time.perf_counter() - t0
+    torch.cuda.synchronize()
+    return {"us": us, "ckpt_bytes": nbytes, "timing": "host clock, launch to copy completion",
+            "copy_after_pass_api": "gdn_prefill_packed + gdn_checkpoint_copy",
+            "overlapped_us": tot / steps * 1e6,
+            "overlapped_api": "gdn_prefill_packed_snapshot (copies start per group of prompts "
+                              "once their checkpoints are stored)"}
 
 
 def run_secondary(torch, gdn, I, h, stream, flush, hbm_gbs):
@@ -474,33 +491,33 @@ def run_secondary(torch, gdn, I, h, stream, flush, hbm_gbs):
     out["decode_32seq"] = {"sequences": B, "us": ms * 1e3, "achieved_gbs": dbytes / (ms / 1e3) / 1e9,
                            "frac_hbm": dbytes / (ms / 1e3) / 1e9 / hbm_gbs}
     # a mixed step: the prompt slices under the 1,024-token budget and the 32 decode tokens,
-    # (a) as a prefill plus a separate decode launch, (b) as one prefill pack in which each
-    # decode token is a one-token segment resuming from its state (the states laid out as
-    # the pack's initial-state array; no gather from a pool is timed)
+    # (a) as a prefill plus a separate decode launch, (b) as one pack in one launch, every
+    # state gathered from and written back to a pool slot (gdn_prefill_packed_pool)
     pre = ms_step.prefill
     pbuf = gdn.to_device(pre)
     ms_two = _time_events(torch, lambda: (gdn.prefill(h, pbuf, stream), gdn.gdn_decode_step(
         h, cfg, B, q, k, v, a, beta, pool, B, slots, o, stream)), stream, flush)
-    lengths = list(pre.lengths) + [1] * B
-    both = I.Pack(name="mixed_one_pack",
-                  cu_seqlens=np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32),
-                  q=np.concatenate([pre.q, ms_step.dec_q]), k=np.concatenate([pre.k, ms_step.dec_k]),
-                  v=np.concatenate([pre.v, ms_step.dec_v]), a=np.concatenate([pre.a, ms_step.dec_a]),
-                  beta=np.concatenate([pre.beta, ms_step.dec_beta]),
-                  init=np.concatenate([np.zeros((pre.num_seqs, 32, 128, 128), np.float32),
-                                       ms_step.dec_states]),
-                  ckpt_cu=np.zeros(len(lengths) + 1, np.int32), ckpt_pos=np.zeros(0, np.int32),
-                  num_k_heads=16, num_v_heads=32, head_dim=128, io_dtype="bf16",
-                  scale=128 ** -0.5)
+    both = I.mixed_one_pack(ms_step)
     obuf = gdn.to_device(both)
-    ms_one = _time_events(torch, lambda: gdn.prefill(h, obuf, stream), stream, flush)
+    nslots = both.num_seqs
+    spool = torch.zeros((nslots, 32, 128, 128), dtype=torch.float32, device="cuda")
+    spool[pre.num_seqs:] = torch.from_numpy(ms_step.dec_states).cuda()
+    slot_idx = list(range(nslots))
+    start_zero = [1] * pre.num_seqs + [0] * B
+    ms_one = _time_events(torch, lambda: gdn.gdn_prefill_packed_pool(
+        h, obuf.cfg, obuf.cu, obuf.q, obuf.k, obuf.v, obuf.a, obuf.beta, spool, nslots,
+        slot_idx, start_zero, obuf.ckpt_cu, None, obuf.o, None, obuf.workspace,
+        obuf.workspace_bytes, stream), stream, flush)
+    launches = gdn.gdn_prefill_launch_count(h)
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     out["mixed_step"] = {
         "prompt_tokens": pre.total_tokens, "decode_tokens": B,
         "prefill_plus_decode_us": ms_two * 1e3, "one_pack_us": ms_one * 1e3,
+        "one_pack_api": "gdn_prefill_packed_pool (states gathered from pool slots)",
+        "one_pack_launches": launches,
         "one_pack_schedule": "throughput" if gdn.gdn_chunked_schedule(
             both.cu_seqlens, 32, sms) == gdn.KERNEL_CHUNKED_THROUGHPUT else "pipelined"}
-    del pbuf, obuf
+    del pbuf, obuf, spool
     return out
 
 

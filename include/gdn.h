@@ -137,13 +137,13 @@ gdn_status gdn_set_test_hook(gdn_handle* handle, int32_t hook);
  * prompts (cu_seqlens_host: prefix sums, as for gdn_prefill_packed) with `num_v_heads`
  * value heads on a GPU with `num_sms` SMs: *schedule = 2 (pipelined) or 3 (throughput),
  * the gdn_set_kernel_preference codes. The choice is the smaller of two estimates from
- * per-chunk costs measured on GB300 (6.4 us per chunk for a pipelined unit on its own SM,
- * 9.5 us for a throughput unit alone on its SM, 11.6 us for one of two sharing an SM), over
- * W = the chunks of all (prompt, value head) units and Lmax = the chunks of the longest,
- * prompts of one token or none left out (their units always run in a launch of their own,
- * with the decode step's arithmetic):
- *   pipelined:  6.4 max(Lmax, W / num_sms)
- *   throughput: max(9.5 Lmax, 11.6 W / (2 num_sms)).
+ * costs measured on GB300 (6.4 us per chunk for a pipelined unit on its own SM, 9.5 us for
+ * a throughput unit alone on its SM, 11.6 us for one of two sharing an SM; 2.0 and 2.5 us
+ * per unit of a prompt with one token or none, which the same launch runs with the decode
+ * step's arithmetic), over W = the chunks of all other (prompt, value head) units, Lmax =
+ * the chunks of the longest and S = the short units:
+ *   pipelined:  max(6.4 Lmax, (6.4 W + 2.0 S) / num_sms)
+ *   throughput: max(9.5 Lmax, (11.6 W + 2.5 S) / (2 num_sms)).
  * Both schedules give bit-identical results; only the time differs. Host-only arithmetic,
  * no CUDA call. Errors: INVALID_ARGUMENT (num_seqs < 0, cu NULL with num_seqs > 0,
  * cu[0] != 0 or decreasing, num_v_heads < 1, num_sms < 1, schedule NULL). */
@@ -197,7 +197,9 @@ gdn_status gdn_prefill_packed(gdn_handle* handle, const gdn_config* cfg, int32_t
  * handle (handle may be NULL: automatic kernel choice), for inspection and tests. Layout,
  * each array on a 256-byte boundary: int32 status, int32 num_units, then num_units units
  * {int32 seq, head, row0, nrows} ordered longest prompt first, then per-prompt records
- * {int32 tok_start, len, ckpt_begin, ckpt_end}, then the checkpoint positions.
+ * {int32 tok_start, len, ckpt_begin, ckpt_end, flags, state_slot}, then the checkpoint
+ * positions, then one int32 per prompt (zero: the checkpoint counters that
+ * gdn_prefill_packed_snapshot's kernels count up).
  * *bytes_needed receives the size; with out == NULL nothing else is written. Errors as
  * gdn_prefill_packed's pack checks, or WORKSPACE_TOO_SMALL when out_bytes is short. */
 gdn_status gdn_prefill_worklist_host(gdn_handle* handle, const gdn_config* cfg,
@@ -219,12 +221,52 @@ gdn_status gdn_read_device_status(const void* workspace, int32_t* status_out, vo
 gdn_status gdn_checkpoint_copy(gdn_handle* handle, const float* ckpt_states_dev, size_t bytes,
                                size_t pool_offset, void* stream);
 
+/* gdn_prefill_packed whose checkpoints are copied into the handle's pinned pool while the
+ * scan still runs ("the scan and the checkpoint copy run on separate streams, not one after
+ * another", sparkinfer v0.6.28 release notes, bullet 2; the pool itself: bullet on pinned
+ * host buffers). Checkpoint slot j lands at byte pool_offset + j * H_v * d * d * 4 of the
+ * pool, the same layout as ckpt_states. Every block of the launch counts its prompt's
+ * stored checkpoints in a per-prompt counter in the workspace; on the handle's side
+ * stream, each copy of a run of prompts (consecutive prompt indices in the work list's
+ * longest-first order, up to 8 MiB) first waits on the device until its prompts' counters
+ * are complete (cuStreamWaitValue32), so the snapshots of prompts that finish early leave
+ * while later prompts are still in the scan. Where the driver offers no stream wait on
+ * memory, one copy follows the whole pass. Outputs are bit-identical to gdn_prefill_packed's.
+ * Completion: gdn_checkpoint_copy_query / _wait on the host, gdn_checkpoint_copy_event or
+ * gdn_checkpoint_copy_join on the device. Arguments and errors as gdn_prefill_packed, plus
+ * POOL_EXHAUSTED when the checkpoints do not fit in the pool at pool_offset. The workspace
+ * must not be reused before the copies have completed. */
+gdn_status gdn_prefill_packed_snapshot(gdn_handle* handle, const gdn_config* cfg,
+                                       int32_t num_seqs, const int32_t* cu_seqlens_host,
+                                       const void* q, const void* k, const void* v,
+                                       const float* a, const float* beta,
+                                       const float* initial_state,
+                                       const int32_t* ckpt_cu_host, const int32_t* ckpt_pos_host,
+                                       void* o, float* ckpt_states, float* final_states,
+                                       size_t pool_offset, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
 /* GDN_OK when every checkpoint copy issued so far has completed, otherwise
  * GDN_ERR_DEVICE_TIMEOUT (not finished yet; nothing is wrong). */
 gdn_status gdn_checkpoint_copy_query(gdn_handle* handle);
 
 /* Block the calling host thread until every checkpoint copy issued so far has completed. */
 gdn_status gdn_checkpoint_copy_wait(gdn_handle* handle);
+
+/* The device-side completion of the checkpoint copies (the scan and the copy on separate
+ * streams, sparkinfer v0.6.28 release notes, bullet 2): *event_out receives the handle's
+ * cudaEvent_t (as void*), recorded on the side stream after the last copy issued so far
+ * by gdn_checkpoint_copy or gdn_prefill_packed_snapshot, so that a consumer stream can
+ * order itself after the snapshots without blocking a host thread
+ * (cudaStreamWaitEvent). The handle owns the event; every later copy call records it
+ * again, so take it after the copies it should cover have been issued. Before any copy it
+ * has never been recorded, and a wait on it completes at once. Errors: INVALID_ARGUMENT. */
+gdn_status gdn_checkpoint_copy_event(gdn_handle* handle, void** event_out);
+
+/* Make `stream` wait on the device for every checkpoint copy issued so far (the same
+ * ordering as a cudaStreamWaitEvent on gdn_checkpoint_copy_event's event); returns at
+ * once. Errors: INVALID_ARGUMENT, CUDA. */
+gdn_status gdn_checkpoint_copy_join(gdn_handle* handle, void* stream);
 
 /* Prefill on the handle's own stream, so that a prefill pass overlaps decode steps that
  * keep running on the caller's streams ("run at most one in-flight prefill on an owned
@@ -296,6 +338,41 @@ gdn_status gdn_prefill_packed_noalloc(const gdn_config* cfg, int32_t num_seqs,
                                       const int32_t* ckpt_cu_host, const int32_t* ckpt_pos_host,
                                       void* o, float* ckpt_states, float* final_states,
                                       void* stream);
+
+/* Mixed step in one launch, with the states gathered from a pool (sparkinfer v0.6.4 release
+ * notes, "What changed": prompt slices under a 1,024-token budget run in the same pass as
+ * the decoding requests; vllm.cpp "vLLM, online serving", lever 2b, packed GDN decode).
+ * gdn_prefill_packed in which every prompt's state lives in a caller-owned pool and is
+ * updated in place: prompt n reads its initial state from state_pool[slot_idx_host[n]]
+ * (or starts from a zero state when start_zero_host is non-NULL and start_zero_host[n] !=
+ * 0) and writes its final state back to the same slot. Decoding sequences ride the pack as
+ * one-token prompts; every (prompt, value head) unit, prompts of one token or none
+ * included, runs in one kernel launch (gdn_prefill_launch_count reports it), so a mixed
+ * step of prompt slices and decode tokens needs no caller-side state copies and no second
+ * launch.
+ *  state_pool       [num_slots][H_v][d][d] fp32 device, 16-byte aligned; slots not named by
+ *                   slot_idx_host are neither read nor written.
+ *  slot_idx_host    [N] int32 host array of distinct slots in [0, num_slots).
+ *  start_zero_host  [N] int32 host array or NULL (NULL: every prompt reads its slot).
+ * Everything else as gdn_prefill_packed (the workspace size is gdn_prefill_workspace_size's).
+ * The pool may not overlap q, k, v, a, beta, o, ckpt_states or the workspace. Errors:
+ * INVALID_ARGUMENT (also for a slot out of range or named twice), UNSUPPORTED,
+ * WORKSPACE_TOO_SMALL, CUDA. */
+gdn_status gdn_prefill_packed_pool(gdn_handle* handle, const gdn_config* cfg, int32_t num_seqs,
+                                   const int32_t* cu_seqlens_host,
+                                   const void* q, const void* k, const void* v,
+                                   const float* a, const float* beta,
+                                   float* state_pool, int32_t num_slots,
+                                   const int32_t* slot_idx_host, const int32_t* start_zero_host,
+                                   const int32_t* ckpt_cu_host, const int32_t* ckpt_pos_host,
+                                   void* o, float* ckpt_states,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Number of kernels that the handle's last prefill call (gdn_prefill_packed and its _pool,
+ * _snapshot, _async, _host and _split forms) enqueued: 1 for any pack of
+ * gdn_prefill_packed, gdn_prefill_packed_pool or gdn_prefill_packed_snapshot with at least
+ * one prompt. Host-side bookkeeping (no CUDA call). Errors: INVALID_ARGUMENT. */
+gdn_status gdn_prefill_launch_count(gdn_handle* handle, int32_t* count);
 
 /* ---- prefill from host memory ---------------------------------------------------------- */
 

@@ -5,6 +5,7 @@
 // is enqueued ("reject unsupported combinations before model loading", pegainfer PR #786,
 // Changes); device work is asynchronous on the caller's stream; the handle owns only host
 // resources, a side stream and events, and destroying it drains that stream first.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -12,6 +13,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -50,6 +52,7 @@ struct gdn_handle {
   int next_slot = 0;
   int32_t kernel_pref = 0;
   int32_t test_hook = 0;  // gdn_set_test_hook
+  int32_t launches = 0;   // kernels enqueued by the last prefill call (gdn_prefill_launch_count)
   // the owned prefill stream: at most one prefill in flight on it
   cudaStream_t prefill_stream = nullptr;
   cudaEvent_t prefill_ready = nullptr;  // caller stream -> prefill stream
@@ -66,10 +69,28 @@ namespace {
 
 gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
 
+// cuStreamWaitValue32 through the runtime's driver entry-point query (once per process).
+using WaitValueFn = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+WaitValueFn wait_value_fn() {
+  static WaitValueFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<WaitValueFn>(f);
+  });
+  return fn;
+}
+
 // Work-list layout inside the workspace (each array on a 256-byte boundary):
-//   header {int32 status; int32 num_units;} | units | seqs | ckpt_pos
+//   header {int32 status; int32 num_units;} | units | seqs | ckpt_pos | ready
+// (ready: one int32 per prompt, zeroed by the upload; gdn_prefill_packed_snapshot's
+// per-prompt checkpoint counters)
 struct ListLayout {
-  size_t units_off, seqs_off, pos_off, total;
+  size_t units_off, seqs_off, pos_off, ready_off, total;
   int32_t num_units;
 };
 
@@ -96,7 +117,8 @@ ListLayout layout_for(int32_t num_seqs, int32_t num_units, int32_t num_ckpt) {
   L.units_off = kAlign;
   L.seqs_off = align_up(L.units_off + sizeof(GdnUnit) * (size_t)num_units, kAlign);
   L.pos_off = align_up(L.seqs_off + sizeof(GdnSeq) * (size_t)num_seqs, kAlign);
-  L.total = align_up(L.pos_off + sizeof(int32_t) * (size_t)std::max(num_ckpt, 1), kAlign);
+  L.ready_off = align_up(L.pos_off + sizeof(int32_t) * (size_t)std::max(num_ckpt, 1), kAlign);
+  L.total = align_up(L.ready_off + sizeof(int32_t) * (size_t)std::max(num_seqs, 1), kAlign);
   return L;
 }
 
@@ -155,9 +177,12 @@ bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
 // Fills the host image of the work list. Units: every (prompt, value head, row block),
 // ordered by prompt length, longest first (stable, so equal lengths keep pack order).
+// Prompt n's state is slot slot_idx[n] of the initial / final state arrays (n without
+// slot_idx); start_zero[n] != 0 makes it start from a zero state.
 void build_worklist(void* dst, const ListLayout& L, KernelFamily fam, const gdn_config* c,
                     int32_t num_seqs, const int32_t* cu, const int32_t* ckpt_cu,
-                    const int32_t* ckpt_pos, int32_t num_ckpt) {
+                    const int32_t* ckpt_pos, int32_t num_ckpt,
+                    const int32_t* slot_idx = nullptr, const int32_t* start_zero = nullptr) {
   std::memset(dst, 0, L.total);
   char* base = static_cast<char*>(dst);
   int32_t* header = reinterpret_cast<int32_t*>(base);
@@ -169,6 +194,8 @@ void build_worklist(void* dst, const ListLayout& L, KernelFamily fam, const gdn_
     seqs[n].len = cu[n + 1] - cu[n];
     seqs[n].ckpt_begin = ckpt_cu ? ckpt_cu[n] : 0;
     seqs[n].ckpt_end = ckpt_cu ? ckpt_cu[n + 1] : 0;
+    seqs[n].flags = start_zero && start_zero[n] ? gdn::kSeqZeroInit : 0;
+    seqs[n].state_slot = slot_idx ? slot_idx[n] : n;
   }
   if (num_ckpt > 0)
     std::memcpy(base + L.pos_off, ckpt_pos, sizeof(int32_t) * (size_t)num_ckpt);
@@ -375,11 +402,13 @@ gdn_status gdn_prefill_workspace_size(const gdn_config* cfg, int32_t num_seqs,
 namespace {
 
 // Pointer, alignment and overlap checks shared by the prefill entry points.
+// `state_slots`: states in the initial / final arrays (num_seqs, or a pool's slot count).
 gdn_status check_buffers(const gdn_config* cfg, int32_t num_seqs, int64_t T, int32_t num_ckpt,
                          const void* q, const void* k, const void* v, const float* a,
                          const float* beta, const float* init, void* o, float* ckpt_states,
                          float* final_states, void* workspace, size_t workspace_bytes,
-                         size_t workspace_needed) {
+                         size_t workspace_needed, int64_t state_slots = -1) {
+  if (state_slots < 0) state_slots = num_seqs;
   const int D = cfg->head_dim_k;
   const size_t es = cfg->io_dtype == GDN_BF16 ? 2 : 4;
   if (T > 0 && (!q || !k || !v || !a || !beta || !o)) return GDN_ERR_INVALID_ARGUMENT;
@@ -399,7 +428,7 @@ gdn_status check_buffers(const gdn_config* cfg, int32_t num_seqs, int64_t T, int
   };
   const Range outs[] = {rng(o, (size_t)T * cfg->num_v_heads * D * es),
                         rng(ckpt_states, (size_t)num_ckpt * state_bytes),
-                        rng(final_states, (size_t)num_seqs * state_bytes)};
+                        rng(final_states, (size_t)state_slots * state_bytes)};
   const Range ins[] = {rng(q, (size_t)T * cfg->num_k_heads * D * es),
                        rng(k, (size_t)T * cfg->num_k_heads * D * es),
                        rng(v, (size_t)T * cfg->num_v_heads * D * es),
@@ -414,7 +443,7 @@ gdn_status check_buffers(const gdn_config* cfg, int32_t num_seqs, int64_t T, int
       if (r.lo && r.hi > r.lo && overlaps(outs[i], r)) return GDN_ERR_INVALID_ARGUMENT;
   }
   if (init && static_cast<const void*>(init) != static_cast<const void*>(final_states)) {
-    const Range ir = rng(init, (size_t)num_seqs * state_bytes);
+    const Range ir = rng(init, (size_t)state_slots * state_bytes);
     for (const Range& r : outs)
       if (r.lo && r.hi > r.lo && overlaps(ir, r)) return GDN_ERR_INVALID_ARGUMENT;
   }
@@ -446,9 +475,10 @@ gdn::PrefillArgs prefill_args(const gdn_config* cfg, const ListLayout& L, char* 
 }
 
 // `load`: the pack's chunk counts, for the chunked kernel's automatic schedule choice.
-int launch_prefill(KernelFamily fam, const gdn_handle* h, const gdn_config* cfg,
+int launch_prefill(KernelFamily fam, gdn_handle* h, const gdn_config* cfg,
                    const gdn::PrefillArgs& pa, int64_t T, const gdn::ChunkLoad& load,
                    void* stream) {
+  if (h && pa.num_units > 0) ++h->launches;  // one kernel launch either way
   if (fam == kChunked) {
     const int schedule = h && h->kernel_pref >= 2 ? h->kernel_pref : gdn::kChunkedAuto;
     gdn::PrefillArgs args = pa;
@@ -476,6 +506,7 @@ gdn_status gdn_prefill_packed(gdn_handle* h, const gdn_config* cfg, int32_t num_
                     final_states, workspace, workspace_bytes, L.total);
   if (s != GDN_OK) return s;
   if (!h) return GDN_ERR_INVALID_ARGUMENT;
+  h->launches = 0;
 
   int prev = 0;
   if (cudaGetDevice(&prev) != cudaSuccess) return GDN_ERR_CUDA;
@@ -502,6 +533,185 @@ gdn_status gdn_prefill_packed(gdn_handle* h, const gdn_config* cfg, int32_t num_
   }
   if (prev != h->device) cudaSetDevice(prev);
   return s;
+}
+
+gdn_status gdn_prefill_packed_pool(gdn_handle* h, const gdn_config* cfg, int32_t num_seqs,
+                                   const int32_t* cu, const void* q, const void* k,
+                                   const void* v, const float* a, const float* beta,
+                                   float* state_pool, int32_t num_slots,
+                                   const int32_t* slot_idx, const int32_t* start_zero,
+                                   const int32_t* ckpt_cu, const int32_t* ckpt_pos, void* o,
+                                   float* ckpt_states, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  KernelFamily fam;
+  ListLayout L;
+  int32_t num_ckpt = 0;
+  gdn_status s = plan(h, cfg, num_seqs, cu, ckpt_cu, ckpt_pos, &fam, &L, &num_ckpt);
+  if (s != GDN_OK) return s;
+  if (!state_pool || num_slots < 1 || !slot_idx) return GDN_ERR_INVALID_ARGUMENT;
+  std::vector<char> taken((size_t)num_slots, 0);
+  for (int32_t n = 0; n < num_seqs; ++n) {
+    const int32_t sl = slot_idx[n];
+    if (sl < 0 || sl >= num_slots || taken[(size_t)sl]) return GDN_ERR_INVALID_ARGUMENT;
+    taken[(size_t)sl] = 1;
+  }
+  const int64_t T = cu[num_seqs];
+  // the pool is both the initial and the final state array (updated in place)
+  s = check_buffers(cfg, num_seqs, T, num_ckpt, q, k, v, a, beta, state_pool, o, ckpt_states,
+                    state_pool, workspace, workspace_bytes, L.total, num_slots);
+  if (s != GDN_OK) return s;
+  if (!h) return GDN_ERR_INVALID_ARGUMENT;
+  h->launches = 0;
+
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (prev != h->device && cudaSetDevice(h->device) != cudaSuccess) return GDN_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  StagingSlot* slot = nullptr;
+  s = take_slot(h, L.total, &slot);
+  if (s == GDN_OK) {
+    build_worklist(slot->host, L, fam, cfg, num_seqs, cu, ckpt_cu, ckpt_pos, num_ckpt, slot_idx,
+                   start_zero);
+    cudaError_t e = cudaMemcpyAsync(workspace, slot->host, L.total, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaEventRecord(slot->done, st);
+    slot->used = true;
+    if (e != cudaSuccess) s = GDN_ERR_CUDA;
+  }
+  if (s == GDN_OK) {
+    char* ws = static_cast<char*>(workspace);
+    const gdn::PrefillArgs pa =
+        prefill_args(cfg, L, ws, reinterpret_cast<int32_t*>(ws), q, k, v, a, beta, state_pool, o,
+                     ckpt_states, state_pool);
+    if (launch_prefill(fam, h, cfg, pa, T, gdn::chunk_load(cu, num_seqs, cfg->num_v_heads),
+                       stream) != 0)
+      s = GDN_ERR_CUDA;
+  }
+  if (prev != h->device) cudaSetDevice(prev);
+  return s;
+}
+
+gdn_status gdn_prefill_packed_snapshot(gdn_handle* h, const gdn_config* cfg, int32_t num_seqs,
+                                       const int32_t* cu, const void* q, const void* k,
+                                       const void* v, const float* a, const float* beta,
+                                       const float* init, const int32_t* ckpt_cu,
+                                       const int32_t* ckpt_pos, void* o, float* ckpt_states,
+                                       float* final_states, size_t pool_offset, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  KernelFamily fam;
+  ListLayout L;
+  int32_t num_ckpt = 0;
+  gdn_status s = plan(h, cfg, num_seqs, cu, ckpt_cu, ckpt_pos, &fam, &L, &num_ckpt);
+  if (s != GDN_OK) return s;
+  const int64_t T = cu[num_seqs];
+  s = check_buffers(cfg, num_seqs, T, num_ckpt, q, k, v, a, beta, init, o, ckpt_states,
+                    final_states, workspace, workspace_bytes, L.total);
+  if (s != GDN_OK) return s;
+  if (!h) return GDN_ERR_INVALID_ARGUMENT;
+  const size_t sb = (size_t)cfg->num_v_heads * cfg->head_dim_v * cfg->head_dim_k * 4;
+  const size_t total = (size_t)num_ckpt * sb;
+  if (pool_offset > h->pool_bytes || total > h->pool_bytes - pool_offset)
+    return GDN_ERR_POOL_EXHAUSTED;
+  WaitValueFn wait = wait_value_fn();
+  h->launches = 0;
+
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (prev != h->device && cudaSetDevice(h->device) != cudaSuccess) return GDN_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  StagingSlot* slot = nullptr;
+  s = take_slot(h, L.total, &slot);
+  cudaError_t e = cudaSuccess;
+  if (s == GDN_OK) {
+    build_worklist(slot->host, L, fam, cfg, num_seqs, cu, ckpt_cu, ckpt_pos, num_ckpt);
+    e = cudaMemcpyAsync(workspace, slot->host, L.total, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaEventRecord(slot->done, st);
+    slot->used = true;
+    // the side stream starts after the upload, which zeroed the prompts' counters
+    if (e == cudaSuccess) e = cudaEventRecord(h->compute_ready, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->compute_ready, 0);
+  }
+  int32_t* ready = reinterpret_cast<int32_t*>(ws + L.ready_off);
+  if (s == GDN_OK && e == cudaSuccess) {
+    gdn::PrefillArgs pa = prefill_args(cfg, L, ws, reinterpret_cast<int32_t*>(ws), q, k, v, a,
+                                       beta, init, o, ckpt_states, final_states);
+    // with the driver's stream wait, every block counts its prompt's stored checkpoints
+    if (wait && num_ckpt > 0) pa.ckpt_ready = ready;
+    if (launch_prefill(fam, h, cfg, pa, T, gdn::chunk_load(cu, num_seqs, cfg->num_v_heads),
+                       stream) != 0)
+      s = GDN_ERR_CUDA;
+  }
+  if (s == GDN_OK && e == cudaSuccess && num_ckpt > 0) {
+    char* dst = static_cast<char*>(h->pool) + pool_offset;
+    const char* src = reinterpret_cast<const char*>(ckpt_states);
+    if (!wait) {
+      // no stream wait on memory: one copy after the whole pass
+      e = cudaEventRecord(h->compute_ready, st);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->compute_ready, 0);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(dst, src, total, cudaMemcpyDeviceToHost, h->side);
+    } else {
+      // prompts in work-list order (longest first, the order in which their blocks start),
+      // runs of consecutive prompt indices (contiguous checkpoint slots) merged up to 8 MiB
+      // per copy; each copy waits until every block of its prompts counted its checkpoints
+      std::vector<int32_t> order(num_seqs);
+      for (int32_t n = 0; n < num_seqs; ++n) order[n] = n;
+      std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) {
+        return (cu[x + 1] - cu[x]) > (cu[y + 1] - cu[y]);
+      });
+      const cuuint32_t target =
+          (cuuint32_t)(cfg->num_v_heads * units_per_head(fam, cfg->head_dim_v));
+      constexpr size_t kCopyBytes = (size_t)8 << 20;
+      size_t i = 0;
+      while (e == cudaSuccess && i < order.size()) {
+        const int32_t n0 = order[i];
+        int32_t n1 = n0 + 1;  // prompts [n0, n1) in this copy
+        size_t j = i + 1;
+        while (j < order.size() && order[j] == n1 &&
+               (size_t)(ckpt_cu[n1 + 1] - ckpt_cu[n0]) * sb <= kCopyBytes) {
+          ++n1;
+          ++j;
+        }
+        const int32_t c0 = ckpt_cu[n0], c1 = ckpt_cu[n1];
+        if (c1 > c0) {
+          for (int32_t n = n0; e == cudaSuccess && n < n1; ++n)
+            if (ckpt_cu[n + 1] > ckpt_cu[n] &&
+                wait(reinterpret_cast<CUstream>(h->side),
+                     reinterpret_cast<CUdeviceptr>(ready + n), target,
+                     CU_STREAM_WAIT_VALUE_GEQ) != CUDA_SUCCESS)
+              e = cudaErrorUnknown;
+          if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dst + (size_t)c0 * sb, src + (size_t)c0 * sb,
+                                (size_t)(c1 - c0) * sb, cudaMemcpyDeviceToHost, h->side);
+        }
+        i = j;
+      }
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(h->copy_done, h->side);
+    if (e == cudaSuccess) h->copy_pending = true;
+  }
+  if (prev != h->device) cudaSetDevice(prev);
+  if (s != GDN_OK) return s;
+  return cuda_status(e);
+}
+
+gdn_status gdn_checkpoint_copy_event(gdn_handle* h, void** event_out) {
+  if (!h || !event_out) return GDN_ERR_INVALID_ARGUMENT;
+  *event_out = static_cast<void*>(h->copy_done);
+  return GDN_OK;
+}
+
+gdn_status gdn_checkpoint_copy_join(gdn_handle* h, void* stream) {
+  if (!h) return GDN_ERR_INVALID_ARGUMENT;
+  if (!h->copy_pending) return GDN_OK;
+  return cuda_status(
+      cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), h->copy_done, 0));
+}
+
+gdn_status gdn_prefill_launch_count(gdn_handle* h, int32_t* count) {
+  if (!h || !count) return GDN_ERR_INVALID_ARGUMENT;
+  *count = h->launches;
+  return GDN_OK;
 }
 
 // ---- prefill from host memory --------------------------------------------------------------
@@ -633,6 +843,7 @@ gdn_status gdn_prefill_packed_host(gdn_handle* h, const gdn_config* cfg, int32_t
     return GDN_ERR_INVALID_ARGUMENT;
   if (!host->final_states || (num_ckpt > 0 && !host->ckpt_states)) return GDN_ERR_INVALID_ARGUMENT;
   if (!host->initial_state != !dev->initial_state) return GDN_ERR_INVALID_ARGUMENT;
+  h->launches = 0;
 
   const size_t es = cfg->io_dtype == GDN_BF16 ? 2 : 4;
   const int D = cfg->head_dim_k;
@@ -751,7 +962,8 @@ void build_vworklist(void* dst, const ListLayout& L, KernelFamily fam, const gdn
   header[1] = L.num_units;
   GdnSeq* seqs = reinterpret_cast<GdnSeq*>(base + L.seqs_off);
   for (size_t n = 0; n < vs.size(); ++n)
-    seqs[n] = GdnSeq{vs[n].tok_start, vs[n].len, vs[n].ckpt_begin, vs[n].ckpt_end, vs[n].flags};
+    seqs[n] = GdnSeq{vs[n].tok_start, vs[n].len, vs[n].ckpt_begin, vs[n].ckpt_end, vs[n].flags,
+                     (int32_t)n};
   if (!pos.empty()) std::memcpy(base + L.pos_off, pos.data(), sizeof(int32_t) * pos.size());
   std::vector<int32_t> order(vs.size());
   for (size_t n = 0; n < vs.size(); ++n) order[n] = (int32_t)n;
@@ -903,6 +1115,7 @@ gdn_status gdn_prefill_packed_split(gdn_handle* h, const gdn_config* cfg, int32_
                     final_states, workspace, workspace_bytes, P.total);
   if (s != GDN_OK) return s;
   if (!h) return GDN_ERR_INVALID_ARGUMENT;
+  h->launches = 0;
 
   int prev = 0;
   if (cudaGetDevice(&prev) != cudaSuccess) return GDN_ERR_CUDA;
@@ -936,6 +1149,7 @@ gdn_status gdn_prefill_packed_split(gdn_handle* h, const gdn_config* cfg, int32_
     // pass A: segment 0 of every prompt and the segment maps of split prompts
     e = gdn::launch_fill_states(init_a, init, reinterpret_cast<const int32_t*>(ws + P.off_fill),
                                 (int)P.va.size(), hv, d, stream);
+    if (!P.va.empty()) ++h->launches;
     if (e == 0)
       e = launch_prefill(fam, h, cfg,
                          prefill_args(cfg, P.la, ws, status, q, k, v, a, beta, init_a, o,
@@ -945,6 +1159,7 @@ gdn_status gdn_prefill_packed_split(gdn_handle* h, const gdn_config* cfg, int32_
     if (e == 0)
       e = gdn::launch_compose_maps(reinterpret_cast<const gdn::SplitCompose*>(ws + P.off_jobs),
                                    (int)P.jobs.size(), fin_a, init_c, hv, d, stream);
+    if (e == 0 && !P.jobs.empty()) ++h->launches;
     if (e == 0 && !P.vc.empty())
       e = launch_prefill(fam, h, cfg,
                          prefill_args(cfg, P.lc, ws + P.off_c, status, q, k, v, a, beta, init_c,
@@ -954,6 +1169,7 @@ gdn_status gdn_prefill_packed_split(gdn_handle* h, const gdn_config* cfg, int32_
       e = gdn::launch_gather_states(final_states, fin_a, fin_c,
                                     reinterpret_cast<const int32_t*>(ws + P.off_gather),
                                     num_seqs, hv, d, stream);
+    if (e == 0) ++h->launches;
     if (e != 0) s = GDN_ERR_CUDA;
   }
   if (prev != h->device) cudaSetDevice(prev);
@@ -1154,6 +1370,7 @@ gdn_status plan_prefill(const gdn_handle* h, const gdn_config* cfg, int32_t num_
   out->units_off = L.units_off;
   out->seqs_off = L.seqs_off;
   out->pos_off = L.pos_off;
+  out->ready_off = L.ready_off;
   out->bytes = L.total;
   out->num_units = L.num_units;
   out->num_ckpt = num_ckpt;
@@ -1166,6 +1383,7 @@ void write_worklist(void* dst, const PrefillPlan& plan, const gdn_config* cfg, i
   L.units_off = plan.units_off;
   L.seqs_off = plan.seqs_off;
   L.pos_off = plan.pos_off;
+  L.ready_off = plan.ready_off;
   L.total = plan.bytes;
   L.num_units = plan.num_units;
   build_worklist(dst, L, static_cast<KernelFamily>(plan.family), cfg, num_seqs, cu, ckpt_cu,

@@ -4,6 +4,7 @@
 // factors (one code path, so that both schedules compute them bit for bit alike) and the
 // warp-level tf32 tile products of the 64 x 64 triangular inverse.
 #pragma once
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <cstdint>
@@ -397,6 +398,125 @@ __device__ __forceinline__ void tile_store_t12(uint8_t* T1, uint8_t* T2, int r0,
     const float2 y1 = ptx::mul2(x, make_float2(g0, g1)), y2 = ptx::mul2(x, make_float2(b0, b1));
     *reinterpret_cast<uint32_t*>(T1 + off) = pack_half2(y1.x, y1.y);
     *reinterpret_cast<uint32_t*>(T2 + off) = pack_half2(y2.x, y2.y);
+  }
+}
+
+// The state of unit (prompt, value head) in the init / final arrays: the prompt's state slot.
+__device__ __forceinline__ size_t state_offset(const PrefillArgs& p, const GdnSeq& sd, int h) {
+  return ((size_t)sd.state_slot * p.hv_heads + h) * kD * kD;
+}
+
+// The initial state of the unit, or nullptr for a zero state.
+__device__ __forceinline__ const float* initial_state(const PrefillArgs& p, const GdnSeq& sd,
+                                                      int h) {
+  return p.init && !(sd.flags & kSeqZeroInit) ? p.init + state_offset(p, sd, h) : nullptr;
+}
+
+// A unit of a prompt with one token or none, run by a whole block of kThreads threads (128,
+// 256 or 512) with the decode step's arithmetic: no chunk phases, no tensor memory (a
+// one-token prompt costs only its state traffic). Both chunked schedules call it, so their
+// results agree bit for bit. Each state row is owned by 4 threads holding 32 entries each
+// as float4 chunks c = sub + 4 m (sub = tid % 4); the block covers kThreads / 4 rows per
+// pass. Every pass's state loads are issued first, so that their latency overlaps the q/k
+// normalisation. The state comes from the prompt's initial state (zero without one) and
+// goes to its final state, and to the prompt's checkpoint when one is requested at
+// position 1; an empty prompt copies its initial state. The initial state may alias the
+// final state: a thread reads each chunk of its rows before it writes it.
+// sk, sq: 128 floats of shared memory each.
+template <int kThreads>
+__device__ __forceinline__ void short_unit(const PrefillArgs& p, const GdnUnit& u,
+                                           const GdnSeq& sd, float* sk, float* sq, int tid) {
+  constexpr int D = kD, kVec = D / 16, kPass = D / (kThreads / 4);
+  static_assert(kPass >= 1 && kPass * (kThreads / 4) == D, "rows per pass");
+  const int h = u.head, hk = h / p.group;
+  const int warp = tid >> 5, lane = tid & 31, sub = tid & 3;
+  const float* init = initial_state(p, sd, h);
+  float* fin = p.final_state + state_offset(p, sd, h);
+  if (sd.len == 0) {  // empty prompt: the final state is the initial state
+    for (int i = tid; i < D * D / 4; i += kThreads)
+      reinterpret_cast<float4*>(fin)[i] =
+          init ? reinterpret_cast<const float4*>(init)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  const size_t tok = (size_t)sd.tok_start;
+  float4 S[kPass][kVec];
+  float vi[kPass];
+#pragma unroll
+  for (int ps = 0; ps < kPass; ++ps) {
+    const int row = ps * (kThreads / 4) + (tid >> 2);
+    const float4* src = init ? reinterpret_cast<const float4*>(init + (size_t)row * D) : nullptr;
+#pragma unroll
+    for (int m = 0; m < kVec; ++m)
+      S[ps][m] = src ? src[sub + 4 * m] : make_float4(0.f, 0.f, 0.f, 0.f);
+    vi[ps] = (sd.flags & kSeqZeroV)
+                 ? 0.f
+                 : __bfloat162float(
+                       static_cast<const __nv_bfloat16*>(p.v)[(tok * p.hv_heads + h) * D + row]);
+  }
+  float ga = p.a[tok * p.hv_heads + h], bb = p.beta[tok * p.hv_heads + h];
+  if (warp == 0) {
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q) + (tok * p.hk_heads + hk) * D;
+    const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(p.k) + (tok * p.hk_heads + hk) * D;
+    float qv[D / 32], kv[D / 32], qq = 0.f, kk = 0.f;
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) {
+      qv[e] = __bfloat162float(q[lane + 32 * e]);
+      kv[e] = __bfloat162float(k[lane + 32 * e]);
+      qq += qv[e] * qv[e];
+      kk += kv[e] * kv[e];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      qq += __shfl_xor_sync(0xffffffffu, qq, off);
+      kk += __shfl_xor_sync(0xffffffffu, kk, off);
+    }
+    const float qs = p.l2norm ? rsqrtf(qq + kL2NormEps) : 1.f;
+    const float ks = p.l2norm ? rsqrtf(kk + kL2NormEps) : 1.f;
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) {
+      sq[lane + 32 * e] = qv[e] * qs;
+      sk[lane + 32 * e] = kv[e] * ks;
+    }
+  }
+  if (p.gate_mode == 1) gate_from_raw(p.a_log[h], p.dt_bias[h], ga, bb);
+  const float g = __expf(ga);
+  __syncthreads();
+  const float4* kr = reinterpret_cast<const float4*>(sk);
+  const float4* qr = reinterpret_cast<const float4*>(sq);
+  const bool ckpt1 = sd.ckpt_end > sd.ckpt_begin && p.ckpt_pos[sd.ckpt_begin] == 1;
+#pragma unroll
+  for (int ps = 0; ps < kPass; ++ps) {
+    const int row = ps * (kThreads / 4) + (tid >> 2);
+    float dot = 0.f;
+#pragma unroll
+    for (int m = 0; m < kVec; ++m) {
+      const float4 k4 = kr[sub + 4 * m];
+      S[ps][m].x *= g; S[ps][m].y *= g; S[ps][m].z *= g; S[ps][m].w *= g;
+      dot += S[ps][m].x * k4.x + S[ps][m].y * k4.y + S[ps][m].z * k4.z + S[ps][m].w * k4.w;
+    }
+    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+    const float delta = bb * (vi[ps] - dot);
+    float4* dst = reinterpret_cast<float4*>(fin + (size_t)row * D);
+    float4* ck = ckpt1 ? reinterpret_cast<float4*>(p.ckpt + ((size_t)sd.ckpt_begin * p.hv_heads + h) *
+                                                              D * D + (size_t)row * D)
+                       : nullptr;
+    float outv = 0.f;
+#pragma unroll
+    for (int m = 0; m < kVec; ++m) {
+      const float4 k4 = kr[sub + 4 * m];
+      const float4 q4 = qr[sub + 4 * m];
+      S[ps][m].x += delta * k4.x; S[ps][m].y += delta * k4.y;
+      S[ps][m].z += delta * k4.z; S[ps][m].w += delta * k4.w;
+      outv += S[ps][m].x * q4.x + S[ps][m].y * q4.y + S[ps][m].z * q4.z + S[ps][m].w * q4.w;
+      dst[sub + 4 * m] = S[ps][m];
+      if (ck) ck[sub + 4 * m] = S[ps][m];
+    }
+    outv += __shfl_xor_sync(0xffffffffu, outv, 1);
+    outv += __shfl_xor_sync(0xffffffffu, outv, 2);
+    if (sub == 0)
+      static_cast<__nv_bfloat16*>(p.o)[(tok * p.hv_heads + h) * D + row] =
+          __float2bfloat16_rn(p.scale * outv);
   }
 }
 

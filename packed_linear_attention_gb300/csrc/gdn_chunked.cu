@@ -272,14 +272,21 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const GdnUnit u = p.units[blockIdx.x];
   const GdnSeq sd = p.seqs[u.seq];
+  if (sd.len <= 1) {  // a prompt of one token or none: the decode step's arithmetic
+    short_unit<kThreads>(p, u, sd, reinterpret_cast<float*>(smem),
+                         reinterpret_cast<float*>(smem) + kD, tid);
+    if (p.ckpt_ready) signal_ckpt_ready(p.ckpt_ready, u.seq, 0, kThreads, tid == 0);
+    return;
+  }
   const int h = u.head, hk = h / p.group;
   const size_t v_stride = (size_t)p.hv_heads * kD;
   __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.o) + (size_t)sd.tok_start * v_stride +
                       (size_t)h * kD;
   const float* ag = p.a + (size_t)sd.tok_start * p.hv_heads + h;
   const float* bg = p.beta + (size_t)sd.tok_start * p.hv_heads + h;
-  const size_t state_off = ((size_t)u.seq * p.hv_heads + h) * kD * kD;
-  const int nchunks = (sd.len + kC - 1) / kC;
+  const size_t state_off = state_offset(p, sd, h);
+  const float* init = initial_state(p, sd, h);
+  const int nchunks = (sd.len + kC - 1) / kC;  // >= 1: len >= 2 here
 
   if (tid == 0) {
     mbar_init(&sm.bar_mma, 1);
@@ -323,7 +330,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
   // ---- initial state -> S32 (scaled by the first chunk's decay) and S16 ----------------
   {
     const float d0 = nchunks > 0 ? sm.next_decay : 1.f;
-    const float* src = p.init ? p.init + state_off + (size_t)row * kD + 64 * half : nullptr;
+    const float* src = init ? init + (size_t)row * kD + 64 * half : nullptr;
 #pragma unroll
     for (int c0 = 0; c0 < 64; c0 += 16) {
       uint32_t r[16], h8[8];
@@ -350,6 +357,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
   bool v_inflight = nchunks > 0 && !vz, mma_inflight = false;
   bool store_pending = false;  // a TMA store of output rows still reading the staging tile
   int c_next = sd.ckpt_begin;
+  bool signaled = false;  // the prompt's ready counter has this block's arrival
 
   for (int c = 0; c < nchunks && ok; ++c) {
     const int t0 = c * kC;
@@ -659,7 +667,14 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       if (emit) ++c_next;
       tmem_st_wait();
       if (L == kC) fence_proxy_async_smem();  // the staged rows go out by TMA
-      __syncthreads();
+      if (p.ckpt_ready && emit && c_next == sd.ckpt_end) {
+        // the unit's last checkpoint is stored: its copy may start (the barrier inside also
+        // orders the staging writes before the store below)
+        signal_ckpt_ready(p.ckpt_ready, u.seq, 0, kThreads, tid == 0);
+        signaled = true;
+      } else {
+        __syncthreads();
+      }
       if (L == kC) {
         // a whole chunk lies inside the prompt: one TMA store of the 64 x 128 tile
         if (tid == 0) {
@@ -684,14 +699,6 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
     tc_fence_after();
   }
 
-  if (ok && sd.len == 0) {
-    // zero-length prompt: the final state is the initial state
-    const float* src = p.init ? p.init + state_off + (size_t)row * kD + 64 * half : nullptr;
-    float* dst = p.final_state + state_off + (size_t)row * kD + 64 * half;
-    for (int e = 0; e < 64; e += 4)
-      *reinterpret_cast<float4*>(dst + e) =
-          src ? __ldg(reinterpret_cast<const float4*>(src + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
   if (!ok) {
     if (tid == 0 && p.status) atomicExch(p.status, kStatusTimeout);
     // let products and copies still in flight land (bounded) before TMEM and shared
@@ -704,6 +711,8 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
     }
   }
   if (tid == 0 && store_pending) bulk_wait_all();  // output stores done before the CTA exits
+  // a unit without checkpoints, or one that gave up before its last, arrives here
+  if (p.ckpt_ready && !signaled) signal_ckpt_ready(p.ckpt_ready, u.seq, 0, kThreads, tid == 0);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tbase, TM_COLS);

@@ -285,12 +285,19 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const GdnUnit u = p.units[blockIdx.x];
   const GdnSeq sd = p.seqs[u.seq];
+  if (sd.len <= 1) {  // a prompt of one token or none: the decode step's arithmetic
+    short_unit<kThreads>(p, u, sd, reinterpret_cast<float*>(smem),
+                         reinterpret_cast<float*>(smem) + kD, tid);
+    if (p.ckpt_ready) signal_ckpt_ready(p.ckpt_ready, u.seq, 0, kThreads, tid == 0);
+    return;
+  }
   const int h = u.head, hk = h / p.group;
   const size_t v_stride = (size_t)p.hv_heads * kD;
   const float* ag = p.a + (size_t)sd.tok_start * p.hv_heads + h;
   const float* bg = p.beta + (size_t)sd.tok_start * p.hv_heads + h;
-  const size_t state_off = ((size_t)u.seq * p.hv_heads + h) * kD * kD;
-  const int nchunks = (sd.len + kC - 1) / kC;
+  const size_t state_off = state_offset(p, sd, h);
+  const float* init = initial_state(p, sd, h);
+  const int nchunks = (sd.len + kC - 1) / kC;  // >= 1: len >= 2 here
   const bool raw = p.gate_mode == 1;
   const float a_log = raw ? __ldg(p.a_log + h) : 0.f;
   const float dt_bias = raw ? __ldg(p.dt_bias + h) : 0.f;
@@ -491,6 +498,7 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
     if (warp == kGateWarp && nchunks > 0) fetch_gates(ag, bg, p.hv_heads, 0, sd.len, lane, gnext);
     bool ok = true, lead_fail = false;
     bool store_pending = false;  // (leader) a TMA store of output rows still reading sO
+    bool signaled = false;       // the prompt's ready counter has this block's arrival
 
     // Gate factors of chunk cc into factor buffer cc & 1 and its total decay into
     // sm.gamma[cc & 1] (gate warp only; published by the next stage_chunk(cc)).
@@ -540,7 +548,7 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
     named_sync(kBarChain, kGroup);
     {
       const float d0 = nchunks > 0 ? sm.gamma[0] : 1.f;
-      const float* src = p.init ? p.init + state_off + (size_t)row * kD + 64 * half : nullptr;
+      const float* src = init ? init + (size_t)row * kD + 64 * half : nullptr;
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 16) {
         uint32_t r[16], h8[8];
@@ -651,6 +659,7 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
       // chunk c+2's q, k into it
       if (leader && c + 2 < nchunks)
         issue_kq(P, sm, smem + OFF_KQ + b * kKQW, b, hk, sd.tok_start + t0 + 2 * kC);
+      bool last_ckpt = false;  // this chunk stores the unit's last checkpoint
       {
         const int pos = t0 + L;
         const bool emit = c_next < sd.ckpt_end && p.ckpt_pos[c_next] == pos;
@@ -692,10 +701,16 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
           }
         }
         if (emit) ++c_next;
+        last_ckpt = emit && c_next == sd.ckpt_end;
         tmem_st_wait();
       }
       tc_fence_before();
-      named_sync(kBarChain, kGroup);
+      if (p.ckpt_ready && last_ckpt) {  // the copy of the prompt's checkpoints may start
+        signal_ckpt_ready(p.ckpt_ready, u.seq, kBarChain, kGroup, leader);
+        signaled = true;
+      } else {
+        named_sync(kBarChain, kGroup);
+      }
       tc_fence_after();
 
       // ---- (C4) next chunk's D^T product now if its operands are ready (else after C5) -------
@@ -778,14 +793,8 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
       if (store_pending) bulk_wait_all();  // output stores done before the CTA exits
     }
 
-    if (ok && sd.len == 0) {
-      // zero-length prompt: the final state is the initial state
-      const float* src = p.init ? p.init + state_off + (size_t)row * kD + 64 * half : nullptr;
-      float* dst = p.final_state + state_off + (size_t)row * kD + 64 * half;
-      for (int e = 0; e < 64; e += 4)
-        *reinterpret_cast<float4*>(dst + e) =
-            src ? __ldg(reinterpret_cast<const float4*>(src + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    // a unit without checkpoints, or one that gave up before its last, arrives here
+    if (p.ckpt_ready && !signaled) signal_ckpt_ready(p.ckpt_ready, u.seq, kBarChain, kGroup, leader);
   }
 
   // ---- both groups done: let every copy and product still in flight land (bounded) --------

@@ -115,101 +115,6 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs p) {
     st_out(static_cast<T*>(p.o) + ((size_t)b * p.hv_heads + h) * D + row, p.scale * outv);
 }
 
-// Units of prompts with one token or none, taken from the prefill work list: four 128-thread
-// blocks per unit (D = 128, bf16 io), 32 state rows each, with decode_kernel's thread mapping
-// and arithmetic. The state comes from the pack's initial states (zero without them) and goes
-// to its final states, and to the prompt's checkpoint when one is requested at position 1;
-// an empty prompt copies its initial state. A one-token prompt would cost the chunked kernel
-// nearly a whole chunk's phases; here it costs its state traffic. The initial state may alias
-// the final state: each thread reads its chunks of a row before it writes them.
-__global__ void __launch_bounds__(kThreads) short_unit_kernel(PrefillArgs p) {
-  constexpr int D = 128, kVec = D / 16;
-  __shared__ __align__(16) float sk[D];
-  __shared__ __align__(16) float sq[D];
-  const GdnUnit u = p.units[blockIdx.x >> 2];
-  const GdnSeq sd = p.seqs[u.seq];
-  const int h = u.head, hk = h / p.group;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r = tid >> 2, sub = tid & 3, row = (blockIdx.x & 3) * 32 + r;
-  const size_t state = ((size_t)u.seq * p.hv_heads + h) * D * D + (size_t)row * D;
-  const float4* src = p.init ? reinterpret_cast<const float4*>(p.init + state) : nullptr;
-  float4 S[kVec];
-#pragma unroll
-  for (int m = 0; m < kVec; ++m) S[m] = src ? src[sub + 4 * m] : make_float4(0.f, 0.f, 0.f, 0.f);
-  float4* fin = reinterpret_cast<float4*>(p.final_state + state);
-  if (sd.len == 0) {  // empty prompt: the final state is the initial state
-#pragma unroll
-    for (int m = 0; m < kVec; ++m) fin[sub + 4 * m] = S[m];
-    return;
-  }
-  const size_t tok = (size_t)sd.tok_start;
-  float ga = p.a[tok * p.hv_heads + h], bb = p.beta[tok * p.hv_heads + h];
-  const float vi = (sd.flags & kSeqZeroV)
-                       ? 0.f
-                       : __bfloat162float(
-                             static_cast<const __nv_bfloat16*>(p.v)[(tok * p.hv_heads + h) * D + row]);
-  if (warp == 0) {
-    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q) + (tok * p.hk_heads + hk) * D;
-    const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(p.k) + (tok * p.hk_heads + hk) * D;
-    float qv[D / 32], kv[D / 32], qq = 0.f, kk = 0.f;
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e) {
-      qv[e] = __bfloat162float(q[lane + 32 * e]);
-      kv[e] = __bfloat162float(k[lane + 32 * e]);
-      qq += qv[e] * qv[e];
-      kk += kv[e] * kv[e];
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      qq += __shfl_xor_sync(0xffffffffu, qq, off);
-      kk += __shfl_xor_sync(0xffffffffu, kk, off);
-    }
-    const float qs = p.l2norm ? rsqrtf(qq + kL2NormEps) : 1.f;
-    const float ks = p.l2norm ? rsqrtf(kk + kL2NormEps) : 1.f;
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e) {
-      sq[lane + 32 * e] = qv[e] * qs;
-      sk[lane + 32 * e] = kv[e] * ks;
-    }
-  }
-  if (p.gate_mode == 1) gate_from_raw(p.a_log[h], p.dt_bias[h], ga, bb);
-  const float g = __expf(ga);
-  __syncthreads();
-
-  const float4* kr = reinterpret_cast<const float4*>(sk);
-  const float4* qr = reinterpret_cast<const float4*>(sq);
-  float dot = 0.f;
-#pragma unroll
-  for (int m = 0; m < kVec; ++m) {
-    const float4 k4 = kr[sub + 4 * m];
-    S[m].x *= g; S[m].y *= g; S[m].z *= g; S[m].w *= g;
-    dot += S[m].x * k4.x + S[m].y * k4.y + S[m].z * k4.z + S[m].w * k4.w;
-  }
-  dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-  dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-  const float delta = bb * (vi - dot);
-  float4* ck = sd.ckpt_end > sd.ckpt_begin && p.ckpt_pos[sd.ckpt_begin] == 1
-                   ? reinterpret_cast<float4*>(p.ckpt + ((size_t)sd.ckpt_begin * p.hv_heads + h) *
-                                                            D * D + (size_t)row * D)
-                   : nullptr;
-  float outv = 0.f;
-#pragma unroll
-  for (int m = 0; m < kVec; ++m) {
-    const float4 k4 = kr[sub + 4 * m];
-    const float4 q4 = qr[sub + 4 * m];
-    S[m].x += delta * k4.x; S[m].y += delta * k4.y;
-    S[m].z += delta * k4.z; S[m].w += delta * k4.w;
-    outv += S[m].x * q4.x + S[m].y * q4.y + S[m].z * q4.z + S[m].w * q4.w;
-    fin[sub + 4 * m] = S[m];
-    if (ck) ck[sub + 4 * m] = S[m];
-  }
-  outv += __shfl_xor_sync(0xffffffffu, outv, 1);
-  outv += __shfl_xor_sync(0xffffffffu, outv, 2);
-  if (sub == 0)
-    static_cast<__nv_bfloat16*>(p.o)[(tok * p.hv_heads + h) * D + row] =
-        __float2bfloat16_rn(p.scale * outv);
-}
-
 }  // namespace
 
 int launch_decode(const DecodeArgs& a, int head_dim, bool bf16, void* stream) {
@@ -226,12 +131,6 @@ int launch_decode(const DecodeArgs& a, int head_dim, bool bf16, void* stream) {
   } else {
     return (int)cudaErrorInvalidValue;
   }
-  return (int)cudaGetLastError();
-}
-
-int launch_short_units(const PrefillArgs& a, void* stream) {
-  if (a.num_units == 0) return 0;
-  short_unit_kernel<<<(unsigned)a.num_units * 4, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
   return (int)cudaGetLastError();
 }
 

@@ -30,9 +30,12 @@ struct GdnSeq {
   int32_t len;         // tokens in the prompt's segment
   int32_t ckpt_begin;  // CSR range of this prompt's checkpoints
   int32_t ckpt_end;
-  int32_t flags;       // kSeqZeroV: v is taken as zero (sequence splitting's map runs)
+  int32_t flags;       // kSeqZeroV, kSeqZeroInit
+  int32_t state_slot;  // index of the prompt's [H_v][d][d] state in init / final_state: the
+                       // prompt's index, or its pool slot (gdn_prefill_packed_pool)
 };
-constexpr int32_t kSeqZeroV = 1;
+constexpr int32_t kSeqZeroV = 1;     // v is taken as zero (sequence splitting's map runs)
+constexpr int32_t kSeqZeroInit = 2;  // the prompt starts from a zero state, whatever init holds
 
 // Everything a prefill kernel needs besides the work list.
 struct PrefillArgs {
@@ -61,7 +64,25 @@ struct PrefillArgs {
   // Test hook (gdn_set_test_hook): the chunked kernels leave out every unit's first q/k
   // copy, so that its first bounded wait runs out and the timeout path runs.
   int32_t test_skip_first_copy = 0;
+  // Per-prompt counters (indexed like seqs) or nullptr. Every block of the launch adds 1 to
+  // its prompt's counter once all of its checkpoint rows are stored and made visible (a
+  // block whose prompt has no checkpoint adds it when it ends), also on the timeout path;
+  // gdn_prefill_packed_snapshot starts each prompt's checkpoint copy from that count.
+  int32_t* ckpt_ready = nullptr;
 };
+
+// Marks a block's checkpoints as stored: every thread that stored checkpoint rows makes its
+// stores visible at system scope, the storing threads meet at barrier `bar_id` (`nthreads`
+// of them, 0 = the block barrier), then `leader` adds 1 to the prompt's counter. Callers
+// skip it (uniformly) when ready is nullptr.
+#ifdef __CUDACC__
+__device__ __forceinline__ void signal_ckpt_ready(int32_t* ready, int32_t seq, uint32_t bar_id,
+                                                  uint32_t nthreads, bool leader) {
+  __threadfence_system();
+  asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(nthreads) : "memory");
+  if (leader) atomicAdd(ready + seq, 1);
+}
+#endif
 
 struct DecodeArgs {
   const void* q;          // [B][Hk][D]
@@ -114,8 +135,8 @@ enum ChunkedSchedule : int { kChunkedAuto = 0, kChunkedPipelined = 2, kChunkedTh
 constexpr int kThroughputCtasPerSM = 2;  // resident throughput CTAs per SM
 
 // Chunk counts of a pack's work list: over all units, and of the longest unit; and the units
-// of prompts with at most one token, which close the longest-first work list and run in a
-// launch of their own (launch_short_units).
+// of prompts with at most one token, which close the longest-first work list and which the
+// chunked kernels run with the decode step's arithmetic (no chunk phases, no tensor memory).
 struct ChunkLoad {
   int64_t total = 0;
   int32_t longest = 0;
@@ -142,9 +163,6 @@ int launch_chunked_throughput(const PrefillArgs& a, int64_t total_tokens, void* 
 int launch_chunked_pipelined(const PrefillArgs& a, int64_t total_tokens, void* stream);
 int launch_chunked_prefill(const PrefillArgs& a, int64_t total_tokens, int schedule,
                            const ChunkLoad& load, void* stream);
-// Units a.units[0 .. a.num_units) of prompts with one token or none (bf16 io, d = 128): the
-// single update on CUDA cores, four 128-thread blocks per unit (gdn_decode.cu).
-int launch_short_units(const PrefillArgs& a, void* stream);
 
 // 2D bf16 tensor maps (64 x 64 boxes, 128-byte swizzle, zero fill past the last row) over
 // q, k (H_k * d columns) and v (H_v * d columns) with total_tokens rows (gdn_tma.cu).
@@ -175,7 +193,7 @@ int launch_gather_states(float* dst, const float* src_a, const float* src_c,
 // the kernel family, the work-list layout and its size for one pack.
 struct PrefillPlan {
   int family;            // 1 = token-serial, 2 = chunked tensor-core
-  size_t units_off, seqs_off, pos_off, bytes;
+  size_t units_off, seqs_off, pos_off, ready_off, bytes;
   int32_t num_units, num_ckpt;
 };
 gdn_status plan_prefill(const gdn_handle* h, const gdn_config* cfg, int32_t num_seqs,

@@ -56,16 +56,17 @@ recurrent_prefill_kernel(PrefillArgs p) {
   const int sub = tid & 3;             // quarter of the row
   const int row = u.row0 + r;
   const bool row_ok = r < u.nrows;
-  const size_t state_row = (((size_t)u.seq * p.hv_heads + h) * D + row) * D;
+  // the prompt's state slot (its index in the pack, or its pool slot)
+  const size_t state_row = (((size_t)sd.state_slot * p.hv_heads + h) * D + row) * D;
+  const bool have_init = p.init != nullptr && !(sd.flags & kSeqZeroInit);
 
   // thread owns float4 chunks c = sub + 4 m of its row (conflict-free smem reads)
   float4 S[kVec];
 #pragma unroll
   for (int m = 0; m < kVec; ++m) {
     const int c = sub + 4 * m;
-    S[m] = (p.init != nullptr && row_ok)
-               ? reinterpret_cast<const float4*>(p.init + state_row)[c]
-               : make_float4(0.f, 0.f, 0.f, 0.f);
+    S[m] = (have_init && row_ok) ? reinterpret_cast<const float4*>(p.init + state_row)[c]
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 
   const T* q = static_cast<const T*>(p.q);
@@ -159,6 +160,8 @@ recurrent_prefill_kernel(PrefillArgs p) {
 #pragma unroll
     for (int m = 0; m < kVec; ++m) dst[sub + 4 * m] = S[m];
   }
+  // this block's checkpoint rows are all stored (the token loop has ended)
+  if (p.ckpt_ready) signal_ckpt_ready(p.ckpt_ready, u.seq, 0, kThreads, tid == 0);
 }
 
 }  // namespace

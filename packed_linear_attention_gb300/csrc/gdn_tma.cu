@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -79,48 +80,59 @@ bool make_qkv_maps(const PrefillArgs& a, int64_t total_tokens, int head_dim, CUt
          make_bf16_map(tv, a.v, (uint64_t)a.hv_heads * head_dim, rows);
 }
 
-// Estimated times from per-chunk costs measured on GB300 with 1,024-token units (tenths of
-// a microsecond per chunk): a pipelined unit on its own SM, a throughput CTA alone on its
-// SM, and a throughput CTA sharing its SM with a second one. A pack takes at least its
-// longest unit's chain and at least its total work spread over the SMs' slots.
+// Estimated times from costs measured on GB300 (tenths of a microsecond): per chunk of a
+// 1,024-token unit, a pipelined unit on its own SM, a throughput CTA alone on its SM and a
+// throughput CTA sharing its SM with a second one; per unit of a prompt with one token or
+// none (the state read and written once by a whole CTA), on a pipelined or throughput CTA
+// slot. A pack takes at least its longest unit's chain and at least its total work spread
+// over the SMs' slots.
 int plan_schedule(const ChunkLoad& load, int32_t num_sms) {
   constexpr double kPipe = 64, kThroughputAlone = 95, kThroughputPaired = 116;
+  constexpr double kShortPipe = 20, kShortThroughput = 25;
   const double longest = load.longest, total = (double)load.total, sms = num_sms;
-  const double t_pipe = kPipe * std::max(longest, total / sms);
-  const double t_thr = std::max(kThroughputAlone * longest,
-                                kThroughputPaired * total / (kThroughputCtasPerSM * sms));
+  const double shorts = (double)load.short_units;
+  const double t_pipe = std::max(kPipe * longest, (kPipe * total + kShortPipe * shorts) / sms);
+  const double t_thr =
+      std::max(kThroughputAlone * longest,
+               (kThroughputPaired * total + kShortThroughput * shorts) /
+                   (kThroughputCtasPerSM * sms));
   return t_thr < t_pipe ? kChunkedThroughput : kChunkedPipelined;
 }
+
+namespace {
+
+// SM count per device, asked once per device; concurrent first calls may each ask, and all
+// store the same value.
+std::atomic<int> g_sms[64];
+
+int device_sms(int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return (int)e;
+  int n = dev >= 0 && dev < 64 ? g_sms[dev].load(std::memory_order_relaxed) : 0;
+  if (n == 0) {
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return (int)e;
+    if (dev >= 0 && dev < 64) g_sms[dev].store(n, std::memory_order_relaxed);
+  }
+  *out = n;
+  return 0;
+}
+
+}  // namespace
 
 int launch_chunked_prefill(const PrefillArgs& a, int64_t total_tokens, int schedule,
                            const ChunkLoad& load, void* stream) {
   if (schedule == kChunkedAuto) {
-    static int sms[64] = {0};  // SM count per device, asked once
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return (int)e;
-    int n = dev >= 0 && dev < 64 ? sms[dev] : 0;
-    if (n == 0) {
-      e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-      if (e != cudaSuccess) return (int)e;
-      if (dev >= 0 && dev < 64) sms[dev] = n;
-    }
+    int n = 0;
+    const int e = device_sms(&n);
+    if (e != 0) return e;
     schedule = plan_schedule(load, n);
   }
-  // prompts with one token or none close the longest-first work list: their units get a
-  // launch of their own, the rest the chunked kernel
-  const int32_t tail = (int32_t)load.short_units;
-  PrefillArgs head = a, rest = a;
-  head.num_units = a.num_units - tail;
-  rest.units = a.units + head.num_units;
-  rest.num_units = tail;
-  if (head.num_units > 0) {
-    const int e = schedule == kChunkedThroughput
-                      ? launch_chunked_throughput(head, total_tokens, stream)
-                      : launch_chunked_pipelined(head, total_tokens, stream);
-    if (e != 0) return e;
-  }
-  return tail > 0 ? launch_short_units(rest, stream) : 0;
+  // one launch for every unit: the units of prompts with one token or none close the
+  // longest-first work list, and the kernels run them with the decode step's arithmetic
+  return schedule == kChunkedThroughput ? launch_chunked_throughput(a, total_tokens, stream)
+                                        : launch_chunked_pipelined(a, total_tokens, stream);
 }
 
 }  // namespace gdn

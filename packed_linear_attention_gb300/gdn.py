@@ -45,7 +45,9 @@ EXPORTS = (
     "gdn_prefill_packed_noalloc", "gdn_prefill_packed_async", "gdn_prefill_async_query",
     "gdn_prefill_async_wait", "gdn_prefill_async_join", "gdn_prefill_split_workspace_size",
     "gdn_prefill_packed_split", "gdn_prefill_packed_host", "gdn_prefill_host_workspace_size",
-    "gdn_chunked_schedule", "gdn_set_test_hook",
+    "gdn_chunked_schedule", "gdn_set_test_hook", "gdn_prefill_packed_pool",
+    "gdn_prefill_launch_count", "gdn_prefill_packed_snapshot", "gdn_checkpoint_copy_event",
+    "gdn_checkpoint_copy_join",
 )
 
 
@@ -99,6 +101,13 @@ def load(path: str = LIB_PATH):
             "gdn_prefill_workspace_size": (I32, [CFG, I32, IP, IP, ctypes.POINTER(SZ)]),
             "gdn_prefill_packed": (I32, [P, CFG, I32, IP, P, P, P, P, P, P, IP, IP, P, P, P,
                                          P, SZ, P]),
+            "gdn_prefill_packed_pool": (I32, [P, CFG, I32, IP, P, P, P, P, P, P, I32, IP, IP,
+                                              IP, IP, P, P, P, SZ, P]),
+            "gdn_prefill_launch_count": (I32, [P, IP]),
+            "gdn_prefill_packed_snapshot": (I32, [P, CFG, I32, IP, P, P, P, P, P, P, IP, IP, P,
+                                                  P, P, SZ, P, SZ, P]),
+            "gdn_checkpoint_copy_event": (I32, [P, ctypes.POINTER(P)]),
+            "gdn_checkpoint_copy_join": (I32, [P, P]),
             "gdn_prefill_split_workspace_size": (I32, [CFG, I32, IP, IP, IP, I32,
                                                        ctypes.POINTER(ctypes.c_size_t)]),
             "gdn_prefill_packed_split": (I32, [P, CFG, I32, IP, P, P, P, P, P, P, IP, IP, P, P,
@@ -243,6 +252,30 @@ def gdn_prefill_packed(handle, cfg, cu_seqlens, q, k, v, a, beta, initial_state,
     return st
 
 
+def gdn_prefill_packed_pool(handle, cfg, cu_seqlens, q, k, v, a, beta, state_pool,
+                            num_slots, slot_idx, start_zero, ckpt_cu, ckpt_pos, o, ckpt_states,
+                            workspace, workspace_bytes, stream=None, *,
+                            raise_on_error=True) -> int:
+    """Prefill whose prompts read and write their states in place in a pool:
+    state_pool[slot_idx[n]] (host int32 list); start_zero[n] != 0 starts prompt n from zeros."""
+    num_seqs = len(cu_seqlens) - 1
+    st = load().gdn_prefill_packed_pool(
+        handle, ctypes.byref(cfg), num_seqs, _i32(cu_seqlens), _addr(q), _addr(k), _addr(v),
+        _addr(a), _addr(beta), _addr(state_pool), int(num_slots), _i32(slot_idx),
+        _i32(start_zero), _i32(ckpt_cu), _i32(ckpt_pos), _addr(o), _addr(ckpt_states),
+        _addr(workspace), int(workspace_bytes), _stream(stream))
+    if raise_on_error:
+        _check(st, "gdn_prefill_packed_pool")
+    return st
+
+
+def gdn_prefill_launch_count(handle) -> int:
+    """Kernels enqueued by the handle's last prefill call."""
+    n = ctypes.c_int32()
+    _check(load().gdn_prefill_launch_count(handle, ctypes.byref(n)), "gdn_prefill_launch_count")
+    return n.value
+
+
 def gdn_prefill_split_workspace_size(cfg: gdn_config, cu_seqlens, ckpt_cu=None, ckpt_pos=None,
                                      segment_len: int = 4096) -> int:
     n = ctypes.c_size_t()
@@ -385,12 +418,14 @@ def gdn_prefill_worklist_host(handle, cfg, cu_seqlens, ckpt_cu=None, ckpt_pos=No
     nu = int(raw[1])
     units_off = 256 // 4
     seqs_off = ((256 + 16 * nu + 255) // 256 * 256) // 4
-    pos_off = ((seqs_off * 4 + 20 * num_seqs + 255) // 256 * 256) // 4  # GdnSeq: 5 int32
+    pos_off = ((seqs_off * 4 + 24 * num_seqs + 255) // 256 * 256) // 4  # GdnSeq: 6 int32
     nck = 0 if ckpt_cu is None else int(np.asarray(ckpt_cu)[-1])
+    ready_off = ((pos_off * 4 + 4 * max(nck, 1) + 255) // 256 * 256) // 4
     return dict(status=int(raw[0]), num_units=nu,
                 units=raw[units_off:units_off + 4 * nu].reshape(nu, 4).copy(),
-                seqs=raw[seqs_off:seqs_off + 5 * num_seqs].reshape(num_seqs, 5).copy(),
-                ckpt_pos=raw[pos_off:pos_off + nck].copy(), nbytes=need.value)
+                seqs=raw[seqs_off:seqs_off + 6 * num_seqs].reshape(num_seqs, 6).copy(),
+                ckpt_pos=raw[pos_off:pos_off + nck].copy(),
+                ready=raw[ready_off:ready_off + num_seqs].copy(), nbytes=need.value)
 
 
 def gdn_read_device_status(workspace, stream=None) -> int:
@@ -405,6 +440,42 @@ def gdn_checkpoint_copy(handle, ckpt_states, nbytes: int, pool_offset: int = 0,
     _check(load().gdn_checkpoint_copy(handle, _addr(ckpt_states), int(nbytes),
                                       int(pool_offset), _stream(stream)),
            "gdn_checkpoint_copy")
+
+
+def gdn_prefill_packed_snapshot(handle, cfg, cu_seqlens, q, k, v, a, beta, initial_state,
+                                ckpt_cu, ckpt_pos, o, ckpt_states, final_states, pool_offset,
+                                workspace, workspace_bytes, stream=None, *,
+                                raise_on_error=True) -> int:
+    """gdn_prefill_packed whose checkpoints are copied into the handle's pinned pool (at
+    pool_offset) while the scan still runs."""
+    st = load().gdn_prefill_packed_snapshot(
+        handle, ctypes.byref(cfg), len(cu_seqlens) - 1, _i32(cu_seqlens), _addr(q), _addr(k),
+        _addr(v), _addr(a), _addr(beta), _addr(initial_state), _i32(ckpt_cu), _i32(ckpt_pos),
+        _addr(o), _addr(ckpt_states), _addr(final_states), int(pool_offset), _addr(workspace),
+        int(workspace_bytes), _stream(stream))
+    if raise_on_error:
+        _check(st, "gdn_prefill_packed_snapshot")
+    return st
+
+
+def prefill_snapshot(handle, buf: "DeviceBuffers", pool_offset: int = 0, stream=None) -> int:
+    """gdn_prefill_packed_snapshot on a DeviceBuffers bundle."""
+    return gdn_prefill_packed_snapshot(handle, buf.cfg, buf.cu, buf.q, buf.k, buf.v, buf.a,
+                                       buf.beta, buf.init, buf.ckpt_cu,
+                                       buf.ckpt_pos if len(buf.ckpt_pos) else None, buf.o,
+                                       buf.ckpt if buf.ckpt.numel() else None, buf.final,
+                                       pool_offset, buf.workspace, buf.workspace_bytes, stream)
+
+
+def gdn_checkpoint_copy_event(handle) -> int:
+    """The handle's copy-completion event (a cudaEvent_t as an integer)."""
+    ev = ctypes.c_void_p()
+    _check(load().gdn_checkpoint_copy_event(handle, ctypes.byref(ev)), "gdn_checkpoint_copy_event")
+    return ev.value or 0
+
+
+def gdn_checkpoint_copy_join(handle, stream=None) -> None:
+    _check(load().gdn_checkpoint_copy_join(handle, _stream(stream)), "gdn_checkpoint_copy_join")
 
 
 def gdn_checkpoint_copy_query(handle) -> bool:

@@ -291,6 +291,25 @@ def mixed_step(seed: int = 0, num_waiting: int = 8, num_decoding: int = 32,
                      dec_k=dk, dec_v=dv, dec_a=da, dec_beta=db, dec_states=ds)
 
 
+def mixed_one_pack(ms: MixedStep) -> Pack:
+    """The mixed step as one pack: the prompt slices (zero initial states) followed by one
+    one-token prompt per decoding sequence (its stored state as initial state)."""
+    pre = ms.prefill
+    B = ms.dec_q.shape[0]
+    lengths = list(pre.lengths) + [1] * B
+    H_v, d = pre.num_v_heads, pre.head_dim
+    return Pack(name="mixed_one_pack",
+                cu_seqlens=np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32),
+                q=np.concatenate([pre.q, ms.dec_q]), k=np.concatenate([pre.k, ms.dec_k]),
+                v=np.concatenate([pre.v, ms.dec_v]), a=np.concatenate([pre.a, ms.dec_a]),
+                beta=np.concatenate([pre.beta, ms.dec_beta]),
+                init=np.concatenate([np.zeros((pre.num_seqs, H_v, d, d), np.float32),
+                                     ms.dec_states]),
+                ckpt_cu=np.zeros(len(lengths) + 1, np.int32), ckpt_pos=np.zeros(0, np.int32),
+                num_k_heads=pre.num_k_heads, num_v_heads=H_v, head_dim=d, io_dtype="bf16",
+                scale=pre.scale)
+
+
 def with_raw_gates(p: Pack, seed: int = 0) -> Pack:
     """The same pack with raw gate projections instead of gates, drawn like a freshly
     initialised Qwen3.5/3.6-style GDN layer: a_raw, b_raw ~ N(0, 1); A = exp(A_log) ~ U(1, 16)

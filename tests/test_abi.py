@@ -209,10 +209,11 @@ def test_chunked_schedule_choice(lib):
         lens = rng.integers(0, 5000, rng.integers(1, 40))
         lens[rng.random(len(lens)) < 0.2] = rng.integers(0, 2)  # empty and one-token prompts
         hv, sms = int(rng.choice([4, 8, 32, 64])), int(rng.choice([1, 132, 152]))
-        ch = np.where(lens > 1, (lens + 63) // 64, 0)  # prompts of <= 1 token run apart
+        ch = np.where(lens > 1, (lens + 63) // 64, 0)  # prompts of <= 1 token: short units
         W, L = float(ch.sum() * hv), float(ch.max())
-        t_pipe = 64 * max(L, W / sms)
-        t_thr = max(95 * L, 116 * W / (2 * sms))
+        S = float((lens <= 1).sum() * hv)
+        t_pipe = max(64 * L, (64 * W + 20 * S) / sms)
+        t_thr = max(95 * L, (116 * W + 25 * S) / (2 * sms))
         assert choose(cu(lens), hv, sms) == (thr if t_thr < t_pipe else pipe)
     for bad in ((cu([3]), 0, 152), (cu([3]), 8, 0), (np.array([1, 4], np.int32), 8, 152),
                 (np.array([0, 4, 2], np.int32), 8, 152)):

@@ -286,7 +286,9 @@ def test_auto_pack_vs_alone_bitwise_across_schedules():
     o, c, f = run(p)
     for n in sorted({0, 1, n_prompts // 2, n_prompts - 1}):
         s = I.sub_pack(p, [n])
-        assert gdn.gdn_chunked_schedule(s.cu_seqlens, 32, sms) == gdn.KERNEL_CHUNKED_PIPELINED
+        if lengths[n] > 1:  # (a one-token prompt runs the same short-unit code either way)
+            assert gdn.gdn_chunked_schedule(s.cu_seqlens, 32, sms) == \
+                gdn.KERNEL_CHUNKED_PIPELINED
         o1, c1, f1 = run(s)
         np.testing.assert_array_equal(o[p.cu_seqlens[n]:p.cu_seqlens[n + 1]], o1)
         np.testing.assert_array_equal(c[p.ckpt_cu[n]:p.ckpt_cu[n + 1]], c1)

@@ -1,0 +1,85 @@
+"""Checkpoint snapshots copied into the handle's pinned pool while the scan still runs
+("the scan and the checkpoint copy run on separate streams, not one after another",
+sparkinfer v0.6.28 release notes, bullet 2): gdn_prefill_packed_snapshot gives the same
+bits as gdn_prefill_packed, the pool holds exactly the device checkpoints, and a consumer
+stream ordered by gdn_checkpoint_copy_join (no host wait) reads the finished snapshots."""
+import numpy as np
+import pytest
+
+from packed_linear_attention_gb300 import gdn
+from packed_linear_attention_gb300 import inputs as I
+
+from gpu_util import handle, run, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def _pool_view(torch, h, nbytes, offset=0):
+    addr, size = gdn.gdn_pool_info(h)
+    assert offset + nbytes <= size
+    import ctypes
+    raw = (ctypes.c_uint8 * nbytes).from_address(addr + offset)
+    return np.frombuffer(raw, dtype=np.uint8)
+
+
+@pytest.mark.parametrize("pack_name", ["ragged", "wave"])
+def test_snapshot_equals_prefill_and_pool_holds_checkpoints(pack_name):
+    torch = torch_cuda()
+    h = handle()
+    p = I.ragged_prefix() if pack_name == "ragged" else I.chat_wave()
+    want = run(p)
+    buf = gdn.to_device(p)
+    nbytes = buf.ckpt.numel() * 4
+    offset = 4096
+    pool = _pool_view(torch, h, nbytes, offset)
+    pool[:] = 0xFF  # NaN bytes: a snapshot that is not written shows
+    gdn.prefill_snapshot(h, buf, offset)
+    gdn.gdn_checkpoint_copy_wait(h)
+    torch.cuda.synchronize()
+    assert gdn.gdn_read_device_status(buf.workspace) == 0
+    assert gdn.gdn_prefill_launch_count(h) == 1
+    got = (buf.o.float().cpu().numpy().astype(np.float64), buf.ckpt.cpu().numpy(),
+           buf.final.cpu().numpy())
+    np.testing.assert_array_equal(got[0], want[0])
+    np.testing.assert_array_equal(got[1].astype(np.float64), want[1])
+    np.testing.assert_array_equal(got[2].astype(np.float64), want[2])
+    np.testing.assert_array_equal(pool.view(np.float32).reshape(got[1].shape), got[1])
+
+
+def test_consumer_stream_joined_on_the_device_sees_the_snapshots():
+    torch = torch_cuda()
+    h = handle()
+    p = I.ragged_prefix()
+    buf = gdn.to_device(p)
+    nbytes = buf.ckpt.numel() * 4
+    pool = _pool_view(torch, h, nbytes)
+    addr, _ = gdn.gdn_pool_info(h)
+    host_src = torch.from_numpy(pool.view(np.uint8))  # the pinned pool as a CPU tensor
+    for rep in range(2):
+        pool[:] = 0xFF
+        consumer = torch.cuda.Stream()
+        dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        gdn.prefill_snapshot(h, buf, 0, torch.cuda.current_stream())
+        gdn.gdn_checkpoint_copy_join(h, consumer)  # device-side ordering only
+        ev = gdn.gdn_checkpoint_copy_event(h)
+        assert ev != 0
+        with torch.cuda.stream(consumer):
+            dst.copy_(host_src, non_blocking=True)  # reads the pinned pool after the join
+        consumer.synchronize()  # the only host wait: on the consumer stream
+        got = dst.cpu().numpy().view(np.float32)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(got, buf.ckpt.cpu().numpy().reshape(-1))
+    assert gdn.gdn_checkpoint_copy_query(h)
+
+
+def test_snapshot_pool_bounds():
+    torch = torch_cuda()
+    h = handle()
+    p = I.ragged_prefix()
+    buf = gdn.to_device(p)
+    _, size = gdn.gdn_pool_info(h)
+    st = gdn.gdn_prefill_packed_snapshot(h, buf.cfg, buf.cu, buf.q, buf.k, buf.v, buf.a,
+                                         buf.beta, buf.init, buf.ckpt_cu, buf.ckpt_pos, buf.o,
+                                         buf.ckpt, buf.final, size - 16, buf.workspace,
+                                         buf.workspace_bytes, raise_on_error=False)
+    assert st == gdn.GDN_ERR_POOL_EXHAUSTED
