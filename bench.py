@@ -232,16 +232,17 @@ def run_reference(args):
     from packed_linear_attention_gb300 import inputs as I
     pack = I.chat_wave()
     threads = os.cpu_count() or 1
-    n_heads = 8
+    # each step: the oracle over the whole wave (every prompt and value head), spread over
+    # all host cores, as the GPU arm's cpu_baseline leg runs it
+    n_prompts, n_heads = pack.num_seqs, pack.num_v_heads
     for _ in range(args.warmup):
-        oracle_rate(pack, 1, n_heads, threads)
+        oracle_rate(pack, n_prompts, n_heads, threads)
     times, desc = [], ""
     for _ in range(args.steps):
-        _, dt, desc = oracle_rate(pack, 1, n_heads, threads)
+        _, dt, desc = oracle_rate(pack, n_prompts, n_heads, threads)
         times.append(dt)
     ms = 1e3 * sum(times) / len(times)
-    layer_tokens = 1024 * n_heads / pack.num_v_heads
-    value = layer_tokens / (ms / 1e3)
+    value = pack.total_tokens / (ms / 1e3)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,

@@ -321,15 +321,20 @@ gdn_status gdn_decode_step(gdn_handle* handle, const gdn_config* cfg, int32_t ba
  * no workspace and no handle argument, and nothing is allocated. The pages describe no
  * such call; it exists for serving engines whose device memory is all handed to their own
  * pool at start-up, and for plugins whose host framework forbids allocation on the request
- * path. Arguments, layouts, results and errors are those of gdn_prefill_packed.
+ * path. Arguments, layouts, results and errors are those of gdn_prefill_packed, except
+ * that a device-side timeout is read with gdn_noalloc_read_status (gdn_read_device_status
+ * needs a workspace).
  * The work list lives in one file-scope device array of GDN_NOALLOC_SCRATCH_BYTES per GPU
  * (held from library load to process exit); a pack whose work list does not fit returns
  * GDN_ERR_UNSUPPORTED before anything is enqueued. Every call rewrites that array and
  * clears its status word, so calls whose device work may overlap in time (two streams)
  * race and must be serialised by the caller. The first call on each device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current; make that
- * first call before any stream capture. The host copy of the work list is taken from a
- * fixed host buffer under a lock (pageable cudaMemcpyAsync). */
+ * first call before any stream capture. That address belongs to the device's primary
+ * context: after a cudaDeviceReset in the same process, do not use this entry point. The
+ * host copy of the work list is taken from one fixed host buffer under one process-wide
+ * lock with a pageable cudaMemcpyAsync, so a call may block the host until work queued
+ * earlier on `stream` has drained, and calls on different GPUs run one after another. */
 gdn_status gdn_prefill_packed_noalloc(const gdn_config* cfg, int32_t num_seqs,
                                       const int32_t* cu_seqlens_host,
                                       const void* q, const void* k, const void* v,
@@ -373,6 +378,18 @@ gdn_status gdn_prefill_packed_pool(gdn_handle* handle, const gdn_config* cfg, in
  * gdn_prefill_packed, gdn_prefill_packed_pool or gdn_prefill_packed_snapshot with at least
  * one prompt. Host-side bookkeeping (no CUDA call). Errors: INVALID_ARGUMENT. */
 gdn_status gdn_prefill_launch_count(gdn_handle* handle, int32_t* count);
+
+/* The status word that the last gdn_prefill_packed_noalloc call on the current device
+ * left (0, or GDN_ERR_DEVICE_TIMEOUT when a bounded device-side wait gave up) into
+ * *status_out: a copy from the fixed device array into the caller's int32 on `stream`,
+ * which it synchronises. No allocation. The pages have no counterpart. Errors:
+ * INVALID_ARGUMENT, UNSUPPORTED (device index beyond 63), CUDA. */
+gdn_status gdn_noalloc_read_status(int32_t* status_out, void* stream);
+
+/* Process-wide test hook of gdn_prefill_packed_noalloc for the device-side timeout path,
+ * with the meaning of gdn_set_test_hook's hook 1 (0 = off, the default). The pages have no
+ * counterpart. Errors: INVALID_ARGUMENT. */
+gdn_status gdn_noalloc_set_test_hook(int32_t hook);
 
 /* ---- prefill from host memory ---------------------------------------------------------- */
 

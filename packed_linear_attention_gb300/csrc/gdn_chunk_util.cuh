@@ -2,7 +2,7 @@
 // kernel (gdn_chunked.cu, gdn_chunked_pipe.cu): fp16 packing into 128B-swizzled operand
 // tiles, the bf16 -> fp16 widening of q/k/v, the gate loads of a chunk, the per-token gate
 // factors (one code path, so that both schedules compute them bit for bit alike) and the
-// warp-level tf32 tile products of the 64 x 64 triangular inverse.
+// warp-level f16 tile products of the 64 x 64 triangular inverse.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -18,8 +18,10 @@ namespace chunk {
 constexpr int kC = 64;          // tokens per chunk
 constexpr int kD = 128;         // head dim
 constexpr int kLd = 68;         // fp32 64x64 matrix row stride (conflict-free float4 rows)
-constexpr int kLdX = 40;        // row stride of the 32 x 32 merge scratch (8 mod 32: its
-                                // tf32 B-fragment loads fall on distinct banks)
+constexpr int kLdX = 36;        // row stride of the 32 x 32 merge scratch (2 kLdX = 8 mod
+                                // 32: its f16 B-fragment loads fall on distinct banks)
+constexpr int kLdXs = 12;       // row stride of a warp's 16 x 8 merge scratch (likewise:
+                                // 2 kLdXs = 24 mod 32 and kLdXs = 12 mod 32)
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr int kStatusTimeout = 5;  // GDN_ERR_DEVICE_TIMEOUT
 constexpr float kLog2e = 1.4426950408889634f;
@@ -180,10 +182,14 @@ __device__ __forceinline__ void convert_kq(uint8_t* sKQ, const Factors& f, int L
     const uint32_t r = pass * 16 + rsub;
     float x[8];
     unpack_bf16x8(w[pass], x);
-    float a = 0.f;
+    // sum of squares of the piece: even and odd elements in two lanes of packed FMAs
+    float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) a = __fmaf_rn(x[e], x[e], a);
-    ss[pass] = a;
+    for (int e = 0; e < 8; e += 2) {
+      const float2 xe = make_float2(x[e], x[e + 1]);
+      a = ptx::fma2(xe, xe, a);
+    }
+    ss[pass] = __fadd_rn(a.x, a.y);
     *at(r) = (int)(r & 63) < L ? pack_half8(x) : make_uint4(0u, 0u, 0u, 0u);
   }
   // reduce-scatter: 8 partial sums -> 4 (xor 8) -> 2 (xor 4) -> 1 (xor 2) -> full (xor 1)
@@ -350,30 +356,34 @@ __device__ __forceinline__ void diag_block_column_rl(const float* A, int o, int 
 }
 
 // One 16 x 8 output tile D += sum_k Ablk[r0.., k] * Bblk[k.., n0..] over k in [k_lo, k_hi)
-// (multiples of 8, at most 32 wide) on one warp, tf32 warp MMAs. Both matrices fp32 with
-// row strides lda/ldb. Each 8-wide k step goes into a zeroed tile of its own and the partial
-// tiles are added in a fixed order, (p0 + p1) + (p2 + p3): the steps run side by side
-// instead of as one chain of dependent warp MMAs, whose latency dominates products this
-// small (measured: 2% on a single 32K-token prompt, neutral elsewhere).
+// (multiples of 16, at most 32 wide) on one warp, f16 warp MMAs (m16n8k16) with fp32
+// accumulation. Both matrices fp32 with row strides lda/ldb, rounded to fp16
+// (round to nearest even) as they are loaded: fp16 keeps tf32's 10-bit significand, and
+// the inverse's entries stay far inside its range. Each 16-wide k step goes into a zeroed
+// tile of its own and the partial tiles are added in a fixed order, so the steps run side
+// by side instead of as a chain of dependent warp MMAs.
 __device__ __forceinline__ void tile_mm(float (&d)[4], const float* Am, int lda, int r0,
                                         const float* Bm, int ldb, int n0, int k_lo, int k_hi,
                                         int gid, int tig) {
-  float p[4][4];
+  float p[2][4];
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
+  for (int s = 0; s < 2; ++s) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) p[s][e] = 0.f;
-    const int k = k_lo + 8 * s;
+    const int k = k_lo + 16 * s;
     if (k < k_hi) {
-      const float a[4] = {Am[(r0 + gid) * lda + k + tig], Am[(r0 + gid + 8) * lda + k + tig],
-                          Am[(r0 + gid) * lda + k + tig + 4],
-                          Am[(r0 + gid + 8) * lda + k + tig + 4]};
-      const float b[2] = {Bm[(k + tig) * ldb + n0 + gid], Bm[(k + tig + 4) * ldb + n0 + gid]};
-      ptx::mma_tf32_f(p[s], a, b);
+      const float* a0 = Am + (r0 + gid) * lda + k + 2 * tig;  // scalar loads: no bank
+      const float* a1 = a0 + 8 * lda;                          // conflicts with lda = 68
+      const uint32_t a[4] = {ptx::f16x2(a0[0], a0[1]), ptx::f16x2(a1[0], a1[1]),
+                             ptx::f16x2(a0[8], a0[9]), ptx::f16x2(a1[8], a1[9])};
+      const float* bc = Bm + n0 + gid;
+      const uint32_t b[2] = {ptx::f16x2(bc[(k + 2 * tig) * ldb], bc[(k + 2 * tig + 1) * ldb]),
+                             ptx::f16x2(bc[(k + 2 * tig + 8) * ldb], bc[(k + 2 * tig + 9) * ldb])};
+      ptx::mma_f16_16816(p[s], a, b);
     }
   }
 #pragma unroll
-  for (int e = 0; e < 4; ++e) d[e] += (p[0][e] + p[1][e]) + (p[2][e] + p[3][e]);
+  for (int e = 0; e < 4; ++e) d[e] += p[0][e] + p[1][e];
 }
 
 // Stores a 16 x 8 accumulator tile (optionally negated) at (r0, n0) of an fp32 matrix.

@@ -17,7 +17,7 @@
 // accumulation; q and k are normalised in fp32 before their rounding, v is widened exactly
 // from bf16, and the fp32 state lives in TMEM for the whole prompt (its fp16 copy feeds
 // the MMAs and is refreshed every chunk). The 64x64 triangular inverse is fp32 (diagonal
-// blocks by forward substitution, off-diagonal blocks by warp-level tf32 products).
+// blocks by forward substitution, off-diagonal blocks by warp-level f16 products).
 // Operands must stay inside the fp16 range (|v| and state entries below 65504).
 //
 // Schedule: one CTA of 16 warps per unit, one CTA per SM, two warp groups in a pipeline.
@@ -71,7 +71,7 @@ static_assert(OFF_D == 131072, "shared-memory map");
 constexpr uint32_t OFF_DP = 147456;     // D'^T (fp16)
 constexpr uint32_t OFF_A = 163840;      // A fp32 [64][68]
 constexpr uint32_t OFF_T = OFF_A + 17408;   // T fp32 [64][68]
-constexpr uint32_t OFF_XS = OFF_T + 17408;  // inverse scratch: 32 x 40 fp32
+constexpr uint32_t OFF_XS = OFF_T + 17408;  // inverse scratch: 32 x kLdX fp32 (5 KB)
 constexpr uint32_t OFF_VEC = OFF_XS + 5120;  // 2 buffers x per-token factors (8 x 64 fp32)
 constexpr uint32_t OFF_T12 = OFF_VEC + 4096;  // T1 | T2 (fp16 64 x 64); blocks above the diagonal stay 0
 constexpr uint32_t SMEM_USED = OFF_T12 + 16384;
@@ -179,8 +179,9 @@ __device__ __forceinline__ void commit(Smem& sm, int i) {
 //  2. (invert_merge) recursive doubling: for L = [[L11, 0], [L21, L22]], L^-1 has
 //     off-diagonal block -L22^-1 L21 L11^-1; first for the 16 x 16 pairs, then for the two
 //     32 x 32 halves.
-// Products run on tf32 warp MMAs: the off-diagonal blocks are small next to the unit
-// diagonal, so their tf32 rounding leaves T within about 1e-6 relative, far below the fp16
+// Products run on f16 warp MMAs (m16n8k16, fp32 accumulation): the off-diagonal blocks are
+// small next to the unit diagonal, so rounding their factors to fp16 (tf32's 10-bit
+// significand) leaves T within about 1e-6 relative, far below the fp16
 // rounding of the operands built from T. Only the lower triangle and the unit diagonal of
 // T are written; blocks of T above the diagonal are never read.
 // Every block of T is also written, as soon as it is known, into the fp16 operands
@@ -212,13 +213,13 @@ __device__ void invert_merge(const float* A, float* T, float* X, uint8_t* T1, ui
   // 16 -> 32: T[16b+16.., 16b..] = -T22 (A21 T11) for b = 0, 2; warps 0-3, one 8-column slice
   if (warp < 4) {
     const int b = 2 * (warp >> 1), r0 = 16 * b + 16, n0 = 16 * b + 8 * (warp & 1);
-    float* xs = X + warp * 128;  // 16 x 8 scratch, row stride 8
+    float* xs = X + warp * 16 * kLdXs;  // 16 x 8 scratch, row stride kLdXs
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     tile_mm(d, A, kLd, r0, T, kLd, n0, 16 * b, 16 * b + 16, gid, tig);
-    tile_store(xs, 8, 0, 0, d, 1.f, gid, tig);
+    tile_store(xs, kLdXs, 0, 0, d, 1.f, gid, tig);
     __syncwarp();
     float y[4] = {0.f, 0.f, 0.f, 0.f};
-    tile_mm(y, T + r0 * kLd + r0, kLd, 0, xs, 8, 0, 0, 16, gid, tig);
+    tile_mm(y, T + r0 * kLd + r0, kLd, 0, xs, kLdXs, 0, 0, 16, gid, tig);
     tile_store(T, kLd, r0, n0, y, -1.f, gid, tig);
     tile_store_t12(T1, T2, r0, n0, y, c1, c2, gid, tig);
   }

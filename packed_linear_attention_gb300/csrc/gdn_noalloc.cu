@@ -16,9 +16,15 @@
 //
 // Set-up: the first call on each device looks up the array's device address with
 // cudaGetSymbolAddress while that device is current, and caches it. Make that first call
-// before any stream capture begins.
+// before any stream capture begins. The cached address belongs to the device's primary
+// context: after a cudaDeviceReset in the same process this entry point must not be used.
+//
+// Status: the array starts with the status word that the chunked kernels set when a
+// bounded device-side wait gives up; gdn_noalloc_read_status copies it into the caller's
+// int32 (no allocation either).
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -35,6 +41,19 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[GDN_NOALLOC_SCRATCH_B
 
 std::mutex g_lock;
 void* g_scratch_addr[kMaxDevices] = {};
+std::atomic<int32_t> g_test_hook{0};  // gdn_noalloc_set_test_hook
+
+// The device address of this device's array (set-up on the first use per device, with that
+// device current). Called with g_lock held.
+gdn_status scratch_address(int dev, char** out) {
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GDN_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = static_cast<char*>(g_scratch_addr[dev]);
+  return GDN_OK;
+}
 // Host image of the work list, copied from pageable memory: cudaMemcpyAsync returns only
 // after the driver has taken the bytes, so the buffer is free again when the lock drops.
 alignas(256) uint8_t g_host_image[GDN_NOALLOC_SCRATCH_BYTES];
@@ -93,12 +112,9 @@ extern "C" gdn_status gdn_prefill_packed_noalloc(const gdn_config* cfg, int32_t 
   if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> guard(g_lock);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GDN_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  char* scratch = static_cast<char*>(g_scratch_addr[dev]);
+  char* scratch = nullptr;
+  const gdn_status sa = scratch_address(dev, &scratch);
+  if (sa != GDN_OK) return sa;
   gdn::write_worklist(g_host_image, plan, cfg, num_seqs, cu, ckpt_cu, ckpt_pos);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(scratch, g_host_image, plan.bytes, cudaMemcpyHostToDevice, st) !=
@@ -121,10 +137,37 @@ extern "C" gdn_status gdn_prefill_packed_noalloc(const gdn_config* cfg, int32_t 
   pa.gate_mode = cfg->gate_mode;
   pa.a_log = cfg->a_log;
   pa.dt_bias = cfg->dt_bias;
+  pa.test_skip_first_copy = g_test_hook.load(std::memory_order_relaxed);
   const int e = plan.family == 2
                     ? gdn::launch_chunked_prefill(pa, T, gdn::kChunkedAuto,
                                                   gdn::chunk_load(cu, num_seqs, cfg->num_v_heads),
                                                   stream)
                     : gdn::launch_recurrent_prefill(pa, D, cfg->io_dtype == GDN_BF16, stream);
   return e == 0 ? GDN_OK : GDN_ERR_CUDA;
+}
+
+extern "C" gdn_status gdn_noalloc_read_status(int32_t* status_out, void* stream) {
+  if (!status_out) return GDN_ERR_INVALID_ARGUMENT;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
+  char* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> guard(g_lock);
+    const gdn_status sa = scratch_address(dev, &scratch);
+    if (sa != GDN_OK) return sa;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, scratch, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GDN_ERR_CUDA;
+  *status_out = v;
+  return GDN_OK;
+}
+
+extern "C" gdn_status gdn_noalloc_set_test_hook(int32_t hook) {
+  if (hook < 0 || hook > 1) return GDN_ERR_INVALID_ARGUMENT;
+  g_test_hook.store(hook, std::memory_order_relaxed);
+  return GDN_OK;
 }

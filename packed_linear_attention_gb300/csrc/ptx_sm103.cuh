@@ -213,30 +213,34 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   return r;
 }
 
-// ---- warp-level tf32 MMA (m16n8k8), used for small fp32 block products -----------------
-
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+// (a.x * b.x + c.x, a.y * b.y + c.y) in one instruction (fma.rn.f32x2), each lane one
+// IEEE fused multiply-add.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{\n .reg .b64 pa, pb, pc, pd;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %5};\n"
+      " mov.b64 pc, {%6, %7};\n fma.rn.f32x2 pd, pa, pb, pc;\n mov.b64 {%0, %1}, pd;\n}\n"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
   return r;
 }
 
-// d += a * b with a: 16x8 (row), b: 8x8 (col) fragments, tf32 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
-                                         const uint32_t (&b)[2]) {
+// ---- warp-level f16 MMA (m16n8k16), used for small block products of the inverse ---------
+
+// Two fp32 values as one f16x2 register (round to nearest even); lo in the low half.
+__device__ __forceinline__ uint32_t f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+// d += a * b with a: 16x16 (row), b: 16x8 (col) f16 fragments, fp32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                              const uint32_t (&b)[2]) {
   asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-// d += a * b with fp32 fragments rounded to tf32 (round to nearest, ties away).
-__device__ __forceinline__ void mma_tf32_f(float (&d)[4], const float (&a)[4],
-                                           const float (&b)[2]) {
-  const uint32_t ah[4] = {to_tf32(a[0]), to_tf32(a[1]), to_tf32(a[2]), to_tf32(a[3])};
-  const uint32_t bh[2] = {to_tf32(b[0]), to_tf32(b[1])};
-  mma_tf32(d, ah, bh);
 }
 
 // ---- fences ------------------------------------------------------------------------------

@@ -47,7 +47,7 @@ EXPORTS = (
     "gdn_prefill_packed_split", "gdn_prefill_packed_host", "gdn_prefill_host_workspace_size",
     "gdn_chunked_schedule", "gdn_set_test_hook", "gdn_prefill_packed_pool",
     "gdn_prefill_launch_count", "gdn_prefill_packed_snapshot", "gdn_checkpoint_copy_event",
-    "gdn_checkpoint_copy_join",
+    "gdn_checkpoint_copy_join", "gdn_noalloc_read_status", "gdn_noalloc_set_test_hook",
 )
 
 
@@ -108,6 +108,8 @@ def load(path: str = LIB_PATH):
                                                   P, P, SZ, P, SZ, P]),
             "gdn_checkpoint_copy_event": (I32, [P, ctypes.POINTER(P)]),
             "gdn_checkpoint_copy_join": (I32, [P, P]),
+            "gdn_noalloc_read_status": (I32, [IP, P]),
+            "gdn_noalloc_set_test_hook": (I32, [I32]),
             "gdn_prefill_split_workspace_size": (I32, [CFG, I32, IP, IP, IP, I32,
                                                        ctypes.POINTER(ctypes.c_size_t)]),
             "gdn_prefill_packed_split": (I32, [P, CFG, I32, IP, P, P, P, P, P, P, IP, IP, P, P,
@@ -344,6 +346,18 @@ def gdn_prefill_packed_noalloc(cfg, cu_seqlens, q, k, v, a, beta, initial_state,
     if raise_on_error:
         _check(st, "gdn_prefill_packed_noalloc")
     return st
+
+
+def gdn_noalloc_read_status(stream=None) -> int:
+    """The status word of the last gdn_prefill_packed_noalloc call on the current device."""
+    v = ctypes.c_int32()
+    _check(load().gdn_noalloc_read_status(ctypes.byref(v), _stream(stream)),
+           "gdn_noalloc_read_status")
+    return v.value
+
+
+def gdn_noalloc_set_test_hook(hook: int) -> None:
+    _check(load().gdn_noalloc_set_test_hook(int(hook)), "gdn_noalloc_set_test_hook")
 
 
 def gdn_prefill_packed_async(handle, cfg, cu_seqlens, q, k, v, a, beta, initial_state, ckpt_cu,

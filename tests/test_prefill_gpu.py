@@ -70,13 +70,14 @@ def test_edge_lengths_d128(pref):
 
 
 @pytest.mark.parametrize("pref", [gdn.KERNEL_AUTO, gdn.KERNEL_CHUNKED_PIPELINED])
-def test_chat_wave_full_size_sampled(wave, pref):
+def test_chat_wave_full_size_every_unit(wave, pref):
     """The 32 x 1,024 wave at full size, in the bench's launch configuration (automatic
-    choice: the throughput schedule) and in the pipelined schedule; sampled prompts and value
-    heads (both members of two GQA groups) against the oracle."""
+    choice: the throughput schedule, whose last SM round is partial) and in the pipelined
+    schedule: every prompt and value head against the oracle, each checkpoint and final
+    state on its own as well as the whole o."""
     torch_cuda()
     got = run(wave, pref)
-    compare_units(wave, got, [0, 13, 31], [0, 1, 30, 31])
+    compare_units(wave, got, list(range(32)), list(range(32)))
 
 
 def test_chat_wave_checkpoint_is_at_768(wave):
@@ -114,11 +115,13 @@ def test_ragged_resume_from_checkpoint_equals_uninterrupted(ragged, pref):
 
 
 @pytest.mark.parametrize("pref", CHUNKED)
-def test_long_prompts_sampled(pref):
+def test_long_prompts_every_unit(pref):
+    """4 x 8,192 tokens (slow decay, checkpoints every 1,024): every prompt and value head
+    against the oracle."""
     torch_cuda()
     p = I.long_prompts()
     got = run(p, pref)
-    compare_units(p, got, [1, 3], [2, 3, 20, 21])
+    compare_units(p, got, list(range(4)), list(range(32)))
 
 
 @pytest.mark.parametrize("pref", KERNELS + CHUNKED)

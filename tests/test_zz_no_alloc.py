@@ -15,13 +15,15 @@ from packed_linear_attention_gb300 import inputs as I
 from gpu_util import assert_close, run, torch_cuda
 
 
-def _noalloc(pack):
+def _noalloc(pack, buf=None):
     torch = torch_cuda()
-    buf = gdn.to_device(pack)
+    if buf is None:
+        buf = gdn.to_device(pack)
     gdn.gdn_prefill_packed_noalloc(buf.cfg, buf.cu, buf.q, buf.k, buf.v, buf.a, buf.beta,
                                    buf.init, buf.ckpt_cu, buf.ckpt_pos, buf.o,
                                    buf.ckpt if buf.ckpt.numel() else None, buf.final)
     torch.cuda.synchronize()
+    assert gdn.gdn_noalloc_read_status() == 0
     return (buf.o.float().cpu().numpy().astype(np.float64),
             buf.ckpt.cpu().numpy().astype(np.float64),
             buf.final.cpu().numpy().astype(np.float64))
@@ -50,6 +52,30 @@ def test_noalloc_token_serial_path_fp32():
     got = _noalloc(p)
     for g, w, what in zip(got, want, ("o", "ckpt", "final")):
         assert_close(g, w, "f32", f"noalloc f32 {what}")
+
+
+@pytest.mark.gpu
+def test_noalloc_reports_a_device_timeout_then_recovers():
+    """The status word of the fixed array is readable without allocating: with the test hook
+    each unit's first copy wait runs out (about a second, no fault) and the status reads
+    GDN_ERR_DEVICE_TIMEOUT; the next call on the same buffers is right and reads 0."""
+    torch = torch_cuda()
+    p = I.make_pack([200, 64, 5], num_k_heads=2, num_v_heads=4, head_dim=128, io_dtype="bf16",
+                    seed=33, ckpt_lists=[[64, 200], [64], []])
+    buf = gdn.to_device(p)
+    gdn.gdn_noalloc_set_test_hook(1)
+    try:
+        gdn.gdn_prefill_packed_noalloc(buf.cfg, buf.cu, buf.q, buf.k, buf.v, buf.a, buf.beta,
+                                       buf.init, buf.ckpt_cu, buf.ckpt_pos, buf.o, buf.ckpt,
+                                       buf.final)
+        assert gdn.gdn_noalloc_read_status() == gdn.GDN_ERR_DEVICE_TIMEOUT
+    finally:
+        gdn.gdn_noalloc_set_test_hook(0)
+    got = _noalloc(p, buf)
+    want = run(p)
+    for g, w, what in zip(got, want, ("o", "ckpt", "final")):
+        assert_close(g, w, "bf16", f"noalloc after timeout {what}")
+    torch.cuda.synchronize()
 
 
 def test_noalloc_rejects_work_lists_beyond_its_array():
