@@ -113,9 +113,10 @@ gdn_status gdn_handle_destroy(gdn_handle* handle);
 gdn_status gdn_pool_info(gdn_handle* handle, void** host_ptr, size_t* bytes);
 
 /* Kernel choice for later prefill calls on this handle:
- *   0 = automatic: the tensor-core chunked kernel where it applies (bf16 io, d = 128),
- *       in the schedule gdn_chunked_schedule names for the pack; otherwise the
- *       token-serial CUDA-core kernel;
+ *   0 = automatic: the tensor-core chunked kernel where it applies (bf16 io, d = 64 or
+ *       128; d = 64 heads run zero-padded to 128, exact), in the schedule
+ *       gdn_chunked_schedule names for the pack; otherwise (fp32 io) the token-serial
+ *       CUDA-core kernel;
  *   1 = always the token-serial kernel (a cross-check path);
  *   2 = the chunked kernel's pipelined schedule, 3 = its throughput schedule (where the
  *       chunked kernel applies; otherwise the token-serial kernel).

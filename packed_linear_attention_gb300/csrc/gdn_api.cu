@@ -96,9 +96,10 @@ struct ListLayout {
 
 enum KernelFamily { kRecurrent = 1, kChunked = 2 };
 
+// bf16 io, d = 64 or 128, C = 64 (d = 64 heads run zero-padded to 128 in the same kernels)
 bool chunked_supported(const gdn_config* c) {
-  return c->io_dtype == GDN_BF16 && c->head_dim_k == 128 && c->head_dim_v == 128 &&
-         c->chunk_size == 64;
+  return c->io_dtype == GDN_BF16 && (c->head_dim_k == 128 || c->head_dim_k == 64) &&
+         c->head_dim_v == c->head_dim_k && c->chunk_size == 64;
 }
 
 KernelFamily pick_kernel(const gdn_handle* h, const gdn_config* c) {
@@ -465,6 +466,7 @@ gdn::PrefillArgs prefill_args(const gdn_config* cfg, const ListLayout& L, char* 
   pa.hk_heads = cfg->num_k_heads;
   pa.hv_heads = cfg->num_v_heads;
   pa.group = cfg->num_v_heads / cfg->num_k_heads;
+  pa.head_dim = cfg->head_dim_k;
   pa.scale = cfg->scale;
   pa.l2norm = cfg->qk_l2norm ? 1 : 0;
   pa.status = status;

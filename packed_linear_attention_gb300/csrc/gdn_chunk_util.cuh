@@ -411,15 +411,18 @@ __device__ __forceinline__ void tile_store_t12(uint8_t* T1, uint8_t* T2, int r0,
   }
 }
 
-// The state of unit (prompt, value head) in the init / final arrays: the prompt's state slot.
+// The state of unit (prompt, value head) in the init / final arrays ([.][H_v][D][D]): the
+// prompt's state slot.
+template <int D>
 __device__ __forceinline__ size_t state_offset(const PrefillArgs& p, const GdnSeq& sd, int h) {
-  return ((size_t)sd.state_slot * p.hv_heads + h) * kD * kD;
+  return ((size_t)sd.state_slot * p.hv_heads + h) * D * D;
 }
 
 // The initial state of the unit, or nullptr for a zero state.
+template <int D>
 __device__ __forceinline__ const float* initial_state(const PrefillArgs& p, const GdnSeq& sd,
                                                       int h) {
-  return p.init && !(sd.flags & kSeqZeroInit) ? p.init + state_offset(p, sd, h) : nullptr;
+  return p.init && !(sd.flags & kSeqZeroInit) ? p.init + state_offset<D>(p, sd, h) : nullptr;
 }
 
 // A unit of a prompt with one token or none, run by a whole block of kThreads threads (128,
@@ -433,15 +436,18 @@ __device__ __forceinline__ const float* initial_state(const PrefillArgs& p, cons
 // position 1; an empty prompt copies its initial state. The initial state may alias the
 // final state: a thread reads each chunk of its rows before it writes it.
 // sk, sq: 128 floats of shared memory each.
-template <int kThreads>
+template <int kThreads, int D>
 __device__ __forceinline__ void short_unit(const PrefillArgs& p, const GdnUnit& u,
                                            const GdnSeq& sd, float* sk, float* sq, int tid) {
-  constexpr int D = kD, kVec = D / 16, kPass = D / (kThreads / 4);
-  static_assert(kPass >= 1 && kPass * (kThreads / 4) == D, "rows per pass");
+  // rows per pass (threads past them idle when the block has more than 4 threads per row)
+  constexpr int kRowsPass = kThreads / 4 < D ? kThreads / 4 : D;
+  constexpr int kVec = D / 16, kPass = D / kRowsPass;
+  static_assert(kPass >= 1 && kPass * kRowsPass == D, "rows per pass");
+  const bool has_row = (tid >> 2) < kRowsPass;
   const int h = u.head, hk = h / p.group;
   const int warp = tid >> 5, lane = tid & 31, sub = tid & 3;
-  const float* init = initial_state(p, sd, h);
-  float* fin = p.final_state + state_offset(p, sd, h);
+  const float* init = initial_state<D>(p, sd, h);
+  float* fin = p.final_state + state_offset<D>(p, sd, h);
   if (sd.len == 0) {  // empty prompt: the final state is the initial state
     for (int i = tid; i < D * D / 4; i += kThreads)
       reinterpret_cast<float4*>(fin)[i] =
@@ -453,7 +459,7 @@ __device__ __forceinline__ void short_unit(const PrefillArgs& p, const GdnUnit& 
   float vi[kPass];
 #pragma unroll
   for (int ps = 0; ps < kPass; ++ps) {
-    const int row = ps * (kThreads / 4) + (tid >> 2);
+    const int row = has_row ? ps * kRowsPass + (tid >> 2) : 0;
     const float4* src = init ? reinterpret_cast<const float4*>(init + (size_t)row * D) : nullptr;
 #pragma unroll
     for (int m = 0; m < kVec; ++m)
@@ -494,9 +500,10 @@ __device__ __forceinline__ void short_unit(const PrefillArgs& p, const GdnUnit& 
   const float4* kr = reinterpret_cast<const float4*>(sk);
   const float4* qr = reinterpret_cast<const float4*>(sq);
   const bool ckpt1 = sd.ckpt_end > sd.ckpt_begin && p.ckpt_pos[sd.ckpt_begin] == 1;
+  if (!has_row) return;  // (whole warps: the row loop shuffles within a warp)
 #pragma unroll
   for (int ps = 0; ps < kPass; ++ps) {
-    const int row = ps * (kThreads / 4) + (tid >> 2);
+    const int row = ps * kRowsPass + (tid >> 2);
     float dot = 0.f;
 #pragma unroll
     for (int m = 0; m < kVec; ++m) {

@@ -19,6 +19,9 @@
 // the MMAs and is refreshed every chunk). The 64x64 triangular inverse is fp32 (diagonal
 // blocks by forward substitution, off-diagonal blocks by warp-level f16 products).
 // Operands must stay inside the fp16 range (|v| and state entries below 65504).
+// Heads of d = 64 run zero-padded to 128: only the first 64-column region of q, k and v is
+// copied in (the other stays zero), so every product sees exact zeros past d and the state
+// rows and columns past d stay zero; only the d x d state and d output columns are stored.
 //
 // Throughput schedule: per CTA (256 threads, 8 warps, two CTAs per SM) one unit, the
 // phases of each chunk in sequence; the two CTAs of an SM hide each other's latencies.
@@ -109,21 +112,20 @@ __device__ __forceinline__ void publish_operands() {
   tc_fence_after();
 }
 
-// Issue the TMA loads of one chunk: q and k (4 boxes, one barrier) and/or v (2 boxes).
+// Issue the TMA loads of one chunk: q and k (one barrier; 2 boxes per 64 columns of d)
+// and/or v (1 box per 64 columns). `dh`: the head dim (64 or 128).
 __device__ __forceinline__ void issue_kq(const ChunkedParams& P, uint8_t* sKQ, uint64_t* bar,
-                                         int hk, int row) {
-  mbar_arrive_expect_tx(bar, KQ_BYTES);
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    tma_load_2d(sKQ + r * 16384, &P.tk, hk * kD + 64 * r, row, bar);
-    tma_load_2d(sKQ + r * 16384 + 8192, &P.tq, hk * kD + 64 * r, row, bar);
+                                         int hk, int row, int dh) {
+  mbar_arrive_expect_tx(bar, KQ_BYTES / (kD / dh));
+  for (int r = 0; r < dh / 64; ++r) {
+    tma_load_2d(sKQ + r * 16384, &P.tk, hk * dh + 64 * r, row, bar);
+    tma_load_2d(sKQ + r * 16384 + 8192, &P.tq, hk * dh + 64 * r, row, bar);
   }
 }
 __device__ __forceinline__ void issue_v(const ChunkedParams& P, uint8_t* sV, uint64_t* bar,
-                                        int h, int row) {
-  mbar_arrive_expect_tx(bar, V_BYTES);
-  tma_load_2d(sV, &P.tv, h * kD, row, bar);
-  tma_load_2d(sV + 8192, &P.tv, h * kD + 64, row, bar);
+                                        int h, int row, int dh) {
+  mbar_arrive_expect_tx(bar, V_BYTES / (kD / dh));
+  for (int r = 0; r < dh / 64; ++r) tma_load_2d(sV + r * 8192, &P.tv, h * dh + 64 * r, row, bar);
 }
 
 
@@ -243,6 +245,7 @@ __device__ void invert_merge(const float* A, float* T, float* X, uint8_t* T1, ui
   }
 }
 
+template <int kDh>  // the head dim d: 128, or 64 (zero-padded to 128)
 __global__ void __launch_bounds__(kThreads, 2)
 chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -273,20 +276,21 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const GdnUnit u = p.units[blockIdx.x];
   const GdnSeq sd = p.seqs[u.seq];
+  constexpr int dh = kDh;
   if (sd.len <= 1) {  // a prompt of one token or none: the decode step's arithmetic
-    short_unit<kThreads>(p, u, sd, reinterpret_cast<float*>(smem),
-                         reinterpret_cast<float*>(smem) + kD, tid);
+    float* sk = reinterpret_cast<float*>(smem);
+    short_unit<kThreads, kDh>(p, u, sd, sk, sk + kD, tid);
     if (p.ckpt_ready) signal_ckpt_ready(p.ckpt_ready, u.seq, 0, kThreads, tid == 0);
     return;
   }
   const int h = u.head, hk = h / p.group;
-  const size_t v_stride = (size_t)p.hv_heads * kD;
+  const size_t v_stride = (size_t)p.hv_heads * dh;
   __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.o) + (size_t)sd.tok_start * v_stride +
-                      (size_t)h * kD;
+                      (size_t)h * dh;
   const float* ag = p.a + (size_t)sd.tok_start * p.hv_heads + h;
   const float* bg = p.beta + (size_t)sd.tok_start * p.hv_heads + h;
-  const size_t state_off = state_offset(p, sd, h);
-  const float* init = initial_state(p, sd, h);
+  const size_t state_off = state_offset<kDh>(p, sd, h);
+  const float* init = initial_state<kDh>(p, sd, h);
   const int nchunks = (sd.len + kC - 1) / kC;  // >= 1: len >= 2 here
 
   if (tid == 0) {
@@ -299,8 +303,14 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       prefetch_tmap(&P.tq);
       prefetch_tmap(&P.tk);
       prefetch_tmap(&P.tv);
-      if (!p.test_skip_first_copy) issue_kq(P, sKQ, &sm.bar_kq, hk, sd.tok_start);
-      if (!(sd.flags & kSeqZeroV)) issue_v(P, sV, &sm.bar_v, h, sd.tok_start);
+      if (!p.test_skip_first_copy) issue_kq(P, sKQ, &sm.bar_kq, hk, sd.tok_start, dh);
+      if (!(sd.flags & kSeqZeroV)) issue_v(P, sV, &sm.bar_v, h, sd.tok_start, dh);
+    }
+  }
+  if (dh == 64) {  // the second 64-column regions of q, k and v are never copied: zeros
+    for (int i = tid; i < 1024; i += kThreads) {
+      *reinterpret_cast<uint4*>(sKQ + 16384 + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+      if (i < 512) *reinterpret_cast<uint4*>(sV + 8192 + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
   if (warp == 0) {
@@ -331,7 +341,10 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
   // ---- initial state -> S32 (scaled by the first chunk's decay) and S16 ----------------
   {
     const float d0 = nchunks > 0 ? sm.next_decay : 1.f;
-    const float* src = init ? init + (size_t)row * kD + 64 * half : nullptr;
+    // (rows and columns past d are zero)
+    const float* src = init && (int)row < dh && 64 * (int)half < dh
+                           ? init + (size_t)row * dh + 64 * half
+                           : nullptr;
 #pragma unroll
     for (int c0 = 0; c0 < 64; c0 += 16) {
       uint32_t r[16], h8[8];
@@ -372,10 +385,10 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
     if (tid == 0 && c + 1 < nchunks) {  // warm L2 with the next chunk's q, k, v
       const int nrow = sd.tok_start + t0 + kC;
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        tma_prefetch_l2_2d(&P.tk, hk * kD + 64 * r, nrow);
-        tma_prefetch_l2_2d(&P.tq, hk * kD + 64 * r, nrow);
-        tma_prefetch_l2_2d(&P.tv, h * kD + 64 * r, nrow);
+      for (int r = 0; r < dh / 64; ++r) {
+        tma_prefetch_l2_2d(&P.tk, hk * dh + 64 * r, nrow);
+        tma_prefetch_l2_2d(&P.tq, hk * dh + 64 * r, nrow);
+        tma_prefetch_l2_2d(&P.tv, h * dh + 64 * r, nrow);
       }
     }
     convert_kq<16384>(sKQ, Factors(sG), L, p.l2norm != 0, tid);  // with the norms
@@ -531,7 +544,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
     if (!(ok = wait_all(&sm.bar_mma, ph_mma, mma_inflight))) break;
     // V and T2 are consumed: fetch the next chunk's v now
     if (tid == 0 && c + 1 < nchunks && !vz) {
-      issue_v(P, sV, &sm.bar_v, h, sd.tok_start + t0 + kC);
+      issue_v(P, sV, &sm.bar_v, h, sd.tok_start + t0 + kC, dh);
       v_inflight = true;
     }
 
@@ -596,7 +609,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
     if (!(ok = wait_all(&sm.bar_mma, ph_mma, mma_inflight))) break;
     // q and k are consumed: fetch the next chunk's
     if (tid == 0 && c + 1 < nchunks) {
-      issue_kq(P, sKQ, &sm.bar_kq, hk, sd.tok_start + t0 + kC);
+      issue_kq(P, sKQ, &sm.bar_kq, hk, sd.tok_start + t0 + kC, dh);
       kq_inflight = true;
     }
 
@@ -622,9 +635,12 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       const bool emit = c_next < sd.ckpt_end && p.ckpt_pos[c_next] == pos;
       const bool last = c + 1 == nchunks;
       const float nd = last ? 1.f : sm.next_decay;
-      float* ck = emit ? p.ckpt + ((size_t)c_next * p.hv_heads + h) * kD * kD + (size_t)row * kD
-                       : nullptr;
-      float* fin = last ? p.final_state + state_off + (size_t)row * kD : nullptr;
+      // (only the d x d state is stored: rows and columns past d are zero)
+      const bool store_row = (int)row < dh;
+      float* ck = emit && store_row
+                      ? p.ckpt + ((size_t)c_next * p.hv_heads + h) * dh * dh + (size_t)row * dh
+                      : nullptr;
+      float* fin = last && store_row ? p.final_state + state_off + (size_t)row * dh : nullptr;
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t s32[32];
@@ -636,17 +652,20 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
           h16[e] = pack_half2(__uint_as_float(s32[2 * e]), __uint_as_float(s32[2 * e + 1]));
         tmem_st16(t_lane + TM_S16 + 32 * half + c0 / 2, h16);
         const int col = 64 * half + c0;
-        if (ck) {
+        const bool store_col = col < dh;
+        if (ck && store_col) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<uint4*>(ck + col + e) =
                 make_uint4(s32[e], s32[e + 1], s32[e + 2], s32[e + 3]);
         }
-        if (fin) {
+        if (last) {
+          if (fin && store_col) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<uint4*>(fin + col + e) =
-                make_uint4(s32[e], s32[e + 1], s32[e + 2], s32[e + 3]);
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<uint4*>(fin + col + e) =
+                  make_uint4(s32[e], s32[e + 1], s32[e + 2], s32[e + 3]);
+          }
         } else {
           uint32_t lo[16], hi[16];
 #pragma unroll
@@ -667,7 +686,8 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       }
       if (emit) ++c_next;
       tmem_st_wait();
-      if (L == kC) fence_proxy_async_smem();  // the staged rows go out by TMA
+      const bool tma_out = L == kC && dh == kD;  // whole d = 128 chunks leave by TMA
+      if (tma_out) fence_proxy_async_smem();
       if (p.ckpt_ready && emit && c_next == sd.ckpt_end) {
         // the unit's last checkpoint is stored: its copy may start (the barrier inside also
         // orders the staging writes before the store below)
@@ -676,7 +696,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       } else {
         __syncthreads();
       }
-      if (L == kC) {
+      if (tma_out) {
         // a whole chunk lies inside the prompt: one TMA store of the 64 x 128 tile
         if (tid == 0) {
           tma_store_2d(&P.to, sO, h * kD, sd.tok_start + t0);
@@ -684,12 +704,13 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
           store_pending = true;
         }
       } else {
-        // the tail chunk: only its L rows (a whole box would reach the next prompt's rows),
-        // by coalesced 16-byte stores
+        // the tail chunk (a whole box would reach the next prompt's rows), or d = 64: only
+        // its L rows and d columns, by coalesced 16-byte stores
+        const int pieces = dh / 8;  // 16-byte pieces of an output row
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
-          const int idx = it * kThreads + tid, t = idx >> 4, ch = idx & 15;
-          if (t < L)
+          const int idx = it * kThreads + tid, t = idx / pieces, ch = idx % pieces;
+          if (t < L && idx < kC * pieces)
             *reinterpret_cast<uint4*>(og + (size_t)(t0 + t) * v_stride + ch * 8) =
                 *reinterpret_cast<const uint4*>(sO + t * 256 + ch * 16);
         }
@@ -725,18 +746,25 @@ int launch_chunked_throughput(const PrefillArgs& a, int64_t total_tokens, void* 
   if (a.num_units == 0) return 0;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(
-        chunked_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-    if (e != cudaSuccess) return (int)e;
+    for (const void* k : {(const void*)chunked_prefill_kernel<128>,
+                          (const void*)chunked_prefill_kernel<64>}) {
+      cudaError_t e =
+          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+      if (e != cudaSuccess) return (int)e;
+    }
     configured = true;
   }
   ChunkedParams P;
   P.a = a;
-  if (!make_qkv_maps(a, total_tokens, kD, &P.tq, &P.tk, &P.tv) ||
-      !make_out_map(&P.to, a.o, (uint64_t)a.hv_heads * kD, (uint64_t)total_tokens))
+  if (!make_qkv_maps(a, total_tokens, a.head_dim, &P.tq, &P.tk, &P.tv) ||
+      !make_out_map(&P.to, a.o, (uint64_t)a.hv_heads * a.head_dim,
+                    a.head_dim == kD ? (uint64_t)total_tokens : 0))
     return (int)cudaErrorInvalidValue;
-  chunked_prefill_kernel<<<a.num_units, kThreads, SMEM_BYTES,
-                                 static_cast<cudaStream_t>(stream)>>>(P);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (a.head_dim == 64)
+    chunked_prefill_kernel<64><<<a.num_units, kThreads, SMEM_BYTES, st>>>(P);
+  else
+    chunked_prefill_kernel<128><<<a.num_units, kThreads, SMEM_BYTES, st>>>(P);
   return (int)cudaGetLastError();
 }
 

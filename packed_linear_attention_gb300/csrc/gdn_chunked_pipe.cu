@@ -19,6 +19,9 @@
 // the MMAs and is refreshed every chunk). The 64x64 triangular inverse is fp32 (diagonal
 // blocks by forward substitution, off-diagonal blocks by warp-level f16 products).
 // Operands must stay inside the fp16 range (|v| and state entries below 65504).
+// Heads of d = 64 run zero-padded to 128: only the first 64-column region of q, k and v is
+// copied in (the other stays zero), so every product sees exact zeros past d and the state
+// rows and columns past d stay zero; only the d x d state and d output columns are stored.
 //
 // Schedule: one CTA of 16 warps per unit, one CTA per SM, two warp groups in a pipeline.
 //   * prep group (warps 0-7): everything of chunk c that does not depend on the state:
@@ -148,24 +151,23 @@ __device__ __forceinline__ void publish(uint32_t bar_id) {
 }
 
 // TMA loads of one chunk: q and k (4 boxes, one barrier) or v (2 boxes).
+// (one region of 64 columns per 64 columns of d: dh = 64 or 128)
 __device__ __forceinline__ void issue_kq(const ChunkedParams& P, Smem& sm, uint8_t* sKQ, int b,
-                                         int hk, int row) {
+                                         int hk, int row, int dh) {
   uint64_t* bar = &sm.bar[B_KQ0 + b];
   ++sm.issued[B_KQ0 + b];
-  mbar_arrive_expect_tx(bar, KQ_BYTES);
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    tma_load_2d(sKQ + r * kRegion, &P.tk, hk * kD + 64 * r, row, bar);
-    tma_load_2d(sKQ + r * kRegion + 8192, &P.tq, hk * kD + 64 * r, row, bar);
+  mbar_arrive_expect_tx(bar, KQ_BYTES / (kD / dh));
+  for (int r = 0; r < dh / 64; ++r) {
+    tma_load_2d(sKQ + r * kRegion, &P.tk, hk * dh + 64 * r, row, bar);
+    tma_load_2d(sKQ + r * kRegion + 8192, &P.tq, hk * dh + 64 * r, row, bar);
   }
 }
 __device__ __forceinline__ void issue_v(const ChunkedParams& P, Smem& sm, uint8_t* sV, int h,
-                                        int row) {
+                                        int row, int dh) {
   uint64_t* bar = &sm.bar[B_V];
   ++sm.issued[B_V];
-  mbar_arrive_expect_tx(bar, V_BYTES);
-  tma_load_2d(sV, &P.tv, h * kD, row, bar);
-  tma_load_2d(sV + 8192, &P.tv, h * kD + 64, row, bar);
+  mbar_arrive_expect_tx(bar, V_BYTES / (kD / dh));
+  for (int r = 0; r < dh / 64; ++r) tma_load_2d(sV + r * 8192, &P.tv, h * dh + 64 * r, row, bar);
 }
 __device__ __forceinline__ void commit(Smem& sm, int i) {
   ++sm.issued[i];
@@ -266,6 +268,7 @@ __device__ __forceinline__ void convert_v(uint8_t* sV, int L, int gtid) {
   }
 }
 
+template <int kDh>  // the head dim d: 128, or 64 (zero-padded to 128)
 __global__ void __launch_bounds__(kThreads, 1)
 chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -286,18 +289,19 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const GdnUnit u = p.units[blockIdx.x];
   const GdnSeq sd = p.seqs[u.seq];
+  constexpr int dh = kDh;
   if (sd.len <= 1) {  // a prompt of one token or none: the decode step's arithmetic
-    short_unit<kThreads>(p, u, sd, reinterpret_cast<float*>(smem),
-                         reinterpret_cast<float*>(smem) + kD, tid);
+    float* sk = reinterpret_cast<float*>(smem);
+    short_unit<kThreads, kDh>(p, u, sd, sk, sk + kD, tid);
     if (p.ckpt_ready) signal_ckpt_ready(p.ckpt_ready, u.seq, 0, kThreads, tid == 0);
     return;
   }
   const int h = u.head, hk = h / p.group;
-  const size_t v_stride = (size_t)p.hv_heads * kD;
+  const size_t v_stride = (size_t)p.hv_heads * dh;
   const float* ag = p.a + (size_t)sd.tok_start * p.hv_heads + h;
   const float* bg = p.beta + (size_t)sd.tok_start * p.hv_heads + h;
-  const size_t state_off = state_offset(p, sd, h);
-  const float* init = initial_state(p, sd, h);
+  const size_t state_off = state_offset<kDh>(p, sd, h);
+  const float* init = initial_state<kDh>(p, sd, h);
   const int nchunks = (sd.len + kC - 1) / kC;  // >= 1: len >= 2 here
   const bool raw = p.gate_mode == 1;
   const float a_log = raw ? __ldg(p.a_log + h) : 0.f;
@@ -318,9 +322,17 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
       prefetch_tmap(&P.tq);
       prefetch_tmap(&P.tk);
       prefetch_tmap(&P.tv);
-      if (!p.test_skip_first_copy) issue_kq(P, sm, smem + OFF_KQ, 0, hk, sd.tok_start);
-      if (!(sd.flags & kSeqZeroV)) issue_v(P, sm, sV, h, sd.tok_start);
-      if (nchunks > 1) issue_kq(P, sm, smem + OFF_KQ + kKQW, 1, hk, sd.tok_start + kC);
+      if (!p.test_skip_first_copy) issue_kq(P, sm, smem + OFF_KQ, 0, hk, sd.tok_start, dh);
+      if (!(sd.flags & kSeqZeroV)) issue_v(P, sm, sV, h, sd.tok_start, dh);
+      if (nchunks > 1) issue_kq(P, sm, smem + OFF_KQ + kKQW, 1, hk, sd.tok_start + kC, dh);
+    }
+  }
+  if (dh == 64) {  // the second 64-column regions of q, k (both buffers) and v: zeros
+    for (int i = tid; i < 1024; i += kThreads) {
+      *reinterpret_cast<uint4*>(smem + OFF_KQ + kRegion + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(smem + OFF_KQ + kKQW + kRegion + 16 * i) =
+          make_uint4(0u, 0u, 0u, 0u);
+      if (i < 512) *reinterpret_cast<uint4*>(sV + 8192 + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
   if (warp == 0) {
@@ -360,10 +372,10 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
       if (leader && c + 2 < nchunks) {  // warm L2 two chunks ahead
         const int nrow = sd.tok_start + t0 + 2 * kC;
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          tma_prefetch_l2_2d(&P.tk, hk * kD + 64 * r, nrow);
-          tma_prefetch_l2_2d(&P.tq, hk * kD + 64 * r, nrow);
-          tma_prefetch_l2_2d(&P.tv, h * kD + 64 * r, nrow);
+        for (int r = 0; r < dh / 64; ++r) {
+          tma_prefetch_l2_2d(&P.tk, hk * dh + 64 * r, nrow);
+          tma_prefetch_l2_2d(&P.tq, hk * dh + 64 * r, nrow);
+          tma_prefetch_l2_2d(&P.tv, h * dh + 64 * r, nrow);
         }
       }
 
@@ -457,7 +469,7 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
       if (!(ok = group_wait(sm, B_M2, c & 1, kBarPrep, leader))) break;
       // V is consumed: fetch the next chunk's
       if (leader && c + 1 < nchunks && !(sd.flags & kSeqZeroV))
-        issue_v(P, sm, sV, h, sd.tok_start + t0 + kC);
+        issue_v(P, sm, sV, h, sd.tok_start + t0 + kC, dh);
 
       // ---- (8) -W -> rows 128-191 of the q/k/w tile (fp16, K-major: rows tokens); hand over ---
       {
@@ -493,7 +505,7 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
     const int ctid = tid - kGroup;
     const bool leader = ctid == 0;
     __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.o) + (size_t)sd.tok_start * v_stride +
-                        (size_t)h * kD;
+                        (size_t)h * dh;
     constexpr int kGateWarp = 15;  // writes every chunk's gate factors, two chunks ahead
     float gnext[4] = {0.f, 0.f, 0.f, 0.f};  // its raw gate loads of the next chunk to stage
     if (warp == kGateWarp && nchunks > 0) fetch_gates(ag, bg, p.hv_heads, 0, sd.len, lane, gnext);
@@ -549,7 +561,10 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
     named_sync(kBarChain, kGroup);
     {
       const float d0 = nchunks > 0 ? sm.gamma[0] : 1.f;
-      const float* src = init ? init + (size_t)row * kD + 64 * half : nullptr;
+      // (rows and columns past d are zero)
+      const float* src = init && (int)row < dh && 64 * (int)half < dh
+                             ? init + (size_t)row * dh + 64 * half
+                             : nullptr;
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 16) {
         uint32_t r[16], h8[8];
@@ -659,15 +674,18 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
       // K and Q~ of buffer b are consumed (the commit covers every earlier product): fetch
       // chunk c+2's q, k into it
       if (leader && c + 2 < nchunks)
-        issue_kq(P, sm, smem + OFF_KQ + b * kKQW, b, hk, sd.tok_start + t0 + 2 * kC);
+        issue_kq(P, sm, smem + OFF_KQ + b * kKQW, b, hk, sd.tok_start + t0 + 2 * kC, dh);
       bool last_ckpt = false;  // this chunk stores the unit's last checkpoint
       {
         const int pos = t0 + L;
         const bool emit = c_next < sd.ckpt_end && p.ckpt_pos[c_next] == pos;
         const float nd = last ? 1.f : sm.gamma[b ^ 1];
-        float* ck = emit ? p.ckpt + ((size_t)c_next * p.hv_heads + h) * kD * kD + (size_t)row * kD
-                         : nullptr;
-        float* fin = last ? p.final_state + state_off + (size_t)row * kD : nullptr;
+        // (only the d x d state is stored: rows and columns past d are zero)
+        const bool store_row = (int)row < dh;
+        float* ck = emit && store_row
+                        ? p.ckpt + ((size_t)c_next * p.hv_heads + h) * dh * dh + (size_t)row * dh
+                        : nullptr;
+        float* fin = last && store_row ? p.final_state + state_off + (size_t)row * dh : nullptr;
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 32) {
           uint32_t s32[32];
@@ -679,17 +697,20 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
             h16[e] = pack_half2(__uint_as_float(s32[2 * e]), __uint_as_float(s32[2 * e + 1]));
           tmem_st16(t_lane + TM_S16 + 32 * half + c0 / 2, h16);
           const int col = 64 * half + c0;
-          if (ck) {
+          const bool store_col = col < dh;
+          if (ck && store_col) {
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
               *reinterpret_cast<uint4*>(ck + col + e) =
                   make_uint4(s32[e], s32[e + 1], s32[e + 2], s32[e + 3]);
           }
-          if (fin) {
+          if (last) {
+            if (fin && store_col) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<uint4*>(fin + col + e) =
-                  make_uint4(s32[e], s32[e + 1], s32[e + 2], s32[e + 3]);
+              for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<uint4*>(fin + col + e) =
+                    make_uint4(s32[e], s32[e + 1], s32[e + 2], s32[e + 3]);
+            }
           } else {
             uint32_t lo[16], hi[16];
 #pragma unroll
@@ -750,10 +771,11 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
         }
         tmem_st_wait();
       }
-      if (L == kC) fence_proxy_async_smem();  // the staged rows go out by TMA
+      const bool tma_out = L == kC && dh == kD;  // whole d = 128 chunks leave by TMA
+      if (tma_out) fence_proxy_async_smem();
       tc_fence_before();
       named_sync(kBarChain, kGroup);
-      if (L == kC) {
+      if (tma_out) {
         // a whole chunk lies inside the prompt: one TMA store of the 64 x 128 tile
         if (leader) {
           tma_store_2d(&P.to, sO, h * kD, sd.tok_start + t0);
@@ -761,12 +783,13 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
           store_pending = true;
         }
       } else {
-        // the tail chunk: only its L rows (a whole box would reach the next prompt's rows),
-        // by coalesced 16-byte stores
+        // the tail chunk (a whole box would reach the next prompt's rows), or d = 64: only
+        // its L rows and d columns, by coalesced 16-byte stores
+        const int pieces = dh / 8;  // 16-byte pieces of an output row
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
-          const int idx = it * kGroup + ctid, t = idx >> 4, ch = idx & 15;
-          if (t < L)
+          const int idx = it * kGroup + ctid, t = idx / pieces, ch = idx % pieces;
+          if (t < L && idx < kC * pieces)
             *reinterpret_cast<uint4*>(og + (size_t)(t0 + t) * v_stride + ch * 8) =
                 *reinterpret_cast<const uint4*>(sO + t * 256 + ch * 16);
         }
@@ -818,18 +841,25 @@ int launch_chunked_pipelined(const PrefillArgs& a, int64_t total_tokens, void* s
   if (a.num_units == 0) return 0;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(
-        chunked_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-    if (e != cudaSuccess) return (int)e;
+    for (const void* k : {(const void*)chunked_pipe_kernel<128>,
+                          (const void*)chunked_pipe_kernel<64>}) {
+      cudaError_t e =
+          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+      if (e != cudaSuccess) return (int)e;
+    }
     configured = true;
   }
   ChunkedParams P;
   P.a = a;
-  if (!make_qkv_maps(a, total_tokens, kD, &P.tq, &P.tk, &P.tv) ||
-      !make_out_map(&P.to, a.o, (uint64_t)a.hv_heads * kD, (uint64_t)total_tokens))
+  if (!make_qkv_maps(a, total_tokens, a.head_dim, &P.tq, &P.tk, &P.tv) ||
+      !make_out_map(&P.to, a.o, (uint64_t)a.hv_heads * a.head_dim,
+                    a.head_dim == kD ? (uint64_t)total_tokens : 0))
     return (int)cudaErrorInvalidValue;
-  chunked_pipe_kernel<<<a.num_units, kThreads, SMEM_BYTES,
-                                 static_cast<cudaStream_t>(stream)>>>(P);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (a.head_dim == 64)
+    chunked_pipe_kernel<64><<<a.num_units, kThreads, SMEM_BYTES, st>>>(P);
+  else
+    chunked_pipe_kernel<128><<<a.num_units, kThreads, SMEM_BYTES, st>>>(P);
   return (int)cudaGetLastError();
 }
 

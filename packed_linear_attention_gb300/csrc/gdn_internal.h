@@ -55,6 +55,7 @@ struct PrefillArgs {
   int32_t hk_heads;
   int32_t hv_heads;
   int32_t group;          // Hv / Hk
+  int32_t head_dim = 128; // d_k = d_v (64 or 128)
   float scale;
   int32_t l2norm;
   int32_t* status;        // device status word (0 = ok) or nullptr

@@ -131,6 +131,7 @@ extern "C" gdn_status gdn_prefill_packed_noalloc(const gdn_config* cfg, int32_t 
   pa.hk_heads = cfg->num_k_heads;
   pa.hv_heads = cfg->num_v_heads;
   pa.group = cfg->num_v_heads / cfg->num_k_heads;
+  pa.head_dim = cfg->head_dim_k;
   pa.scale = cfg->scale;
   pa.l2norm = cfg->qk_l2norm ? 1 : 0;
   pa.status = reinterpret_cast<int32_t*>(scratch);

@@ -55,6 +55,42 @@ def test_tiny_dims_bf16(pref):
 
 
 @pytest.mark.parametrize("pref", KERNELS + CHUNKED)
+def test_d64_bf16_on_both_chunked_schedules(pref):
+    """d = 64 bf16 heads through the tensor-core kernel (zero-padded to 128) in both
+    schedules and through the token-serial kernel: every prompt and head against the
+    oracle, edge lengths, initial states, checkpoints on and off the 64-token grid ends."""
+    torch_cuda()
+    lengths = [1, 0, 2, 63, 64, 65, 129, 200, 330]
+    ck = [[q for q in range(64, n + 1, 64)] + ([n] if n % 64 and n > 0 else []) for n in lengths]
+    p = I.make_pack(lengths, num_k_heads=4, num_v_heads=8, head_dim=64, io_dtype="bf16",
+                    seed=12, init_std=0.02, ckpt_lists=ck)
+    got = run(p, pref)
+    compare_units(p, got, list(range(len(lengths))), list(range(8)))
+
+
+def test_d64_bf16_schedules_bitwise_and_pack_vs_alone():
+    """d = 64 bf16: the two chunked schedules agree bit for bit, and each prompt's o,
+    checkpoints and final state are identical alone and in the pack."""
+    torch_cuda()
+    lengths = [300, 1, 77, 64, 150]
+    ck = [[64, 256], [1], [77], [64], [128, 150]]
+    p = I.make_pack(lengths, num_k_heads=2, num_v_heads=4, head_dim=64, io_dtype="bf16",
+                    seed=13, init_std=0.02, ckpt_lists=ck)
+    a = run(p, gdn.KERNEL_CHUNKED_PIPELINED)
+    b = run(p, gdn.KERNEL_CHUNKED_THROUGHPUT)
+    c = run(p)
+    for x, y, z in zip(a, b, c):
+        np.testing.assert_array_equal(x, y)
+        np.testing.assert_array_equal(x, z)
+    for n in range(len(lengths)):
+        s = I.sub_pack(p, [n])
+        o1, c1, f1 = run(s)
+        np.testing.assert_array_equal(c[0][p.cu_seqlens[n]:p.cu_seqlens[n + 1]], o1)
+        np.testing.assert_array_equal(c[1][p.ckpt_cu[n]:p.ckpt_cu[n + 1]], c1)
+        np.testing.assert_array_equal(c[2][n], f1[0])
+
+
+@pytest.mark.parametrize("pref", KERNELS + CHUNKED)
 def test_edge_lengths_d128(pref):
     """Empty prompts, single tokens, chunk-1/chunk/chunk+1 tails, checkpoints at ends."""
     torch_cuda()
