@@ -477,6 +477,20 @@ gdn_status gdn_prefill_packed_split(gdn_handle* handle, const gdn_config* cfg,
                                     float* final_states, int32_t segment_len, void* workspace,
                                     size_t workspace_bytes, void* stream);
 
+/* The segment length for gdn_prefill_packed_split that the chunked kernels' cost model
+ * (the per-chunk costs of gdn_chunked_schedule) expects to run this pack fastest, or 0 when
+ * splitting is not expected to pay (then call gdn_prefill_packed). It compares the whole
+ * pack in one launch with P = 2 .. 16 segments of the longest prompt (each a multiple of
+ * 64): pass 1 with segment 0 of every prompt plus two map runs per middle segment, pass 2
+ * with the later segments, and 12 us for the extra launches. Splitting shortens the longest
+ * chain of chunks, so it pays for packs with few (prompt, value head) units per SM and one
+ * long prompt, such as one 32K prompt or a ragged pack with one long prompt; the choice
+ * depends on the whole pack, so results split this way carry the split path's rounding
+ * (gdn_prefill_packed_split) rather than being bit-identical to gdn_prefill_packed's.
+ * Host-only, no CUDA call. Errors: INVALID_ARGUMENT (as gdn_chunked_schedule). */
+gdn_status gdn_split_segment_auto(int32_t num_seqs, const int32_t* cu_seqlens_host,
+                                  int32_t num_v_heads, int32_t num_sms, int32_t* segment_len);
+
 /* ---- host-side scheduling policy (no device work) ---------------------------------- */
 
 /* Prefix-cache checkpoint position of a prompt of `len` tokens on a grid of `block`

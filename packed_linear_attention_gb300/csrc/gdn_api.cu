@@ -1083,6 +1083,17 @@ gdn_status plan_split(int32_t pref, const gdn_config* cfg, int32_t num_seqs, con
 
 }  // namespace
 
+gdn_status gdn_split_segment_auto(int32_t num_seqs, const int32_t* cu, int32_t num_v_heads,
+                                  int32_t num_sms, int32_t* segment_len) {
+  if (num_seqs < 0 || (num_seqs > 0 && !cu) || num_v_heads < 1 || num_sms < 1 || !segment_len)
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (num_seqs > 0 && cu[0] != 0) return GDN_ERR_INVALID_ARGUMENT;
+  for (int32_t n = 0; n < num_seqs; ++n)
+    if (cu[n + 1] < cu[n]) return GDN_ERR_INVALID_ARGUMENT;
+  *segment_len = gdn::choose_split_segment(cu, num_seqs, num_v_heads, num_sms);
+  return GDN_OK;
+}
+
 gdn_status gdn_prefill_split_workspace_size(const gdn_config* cfg, int32_t num_seqs,
                                             const int32_t* cu_seqlens_host,
                                             const int32_t* ckpt_cu_host,

@@ -160,6 +160,12 @@ inline ChunkLoad chunk_load(const int32_t* cu, int32_t num_seqs, int32_t units_p
 }
 // kChunkedPipelined or kChunkedThroughput for a pack of this load on `num_sms` SMs.
 int plan_schedule(const ChunkLoad& load, int32_t num_sms);
+// The cost model's estimate (microseconds) of one chunked launch over this load.
+double estimate_pass_us(const ChunkLoad& load, int32_t num_sms);
+// The segment length (a multiple of 64) that the cost model expects to run a pack fastest
+// through sequence splitting, or 0 when splitting is not expected to pay.
+int32_t choose_split_segment(const int32_t* cu, int32_t num_seqs, int32_t num_v_heads,
+                             int32_t num_sms);
 int launch_chunked_throughput(const PrefillArgs& a, int64_t total_tokens, void* stream);
 int launch_chunked_pipelined(const PrefillArgs& a, int64_t total_tokens, void* stream);
 int launch_chunked_prefill(const PrefillArgs& a, int64_t total_tokens, int schedule,

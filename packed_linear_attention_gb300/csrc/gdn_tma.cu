@@ -86,17 +86,73 @@ bool make_qkv_maps(const PrefillArgs& a, int64_t total_tokens, int head_dim, CUt
 // none (the state read and written once by a whole CTA), on a pipelined or throughput CTA
 // slot. A pack takes at least its longest unit's chain and at least its total work spread
 // over the SMs' slots.
-int plan_schedule(const ChunkLoad& load, int32_t num_sms) {
+namespace {
+
+void schedule_estimates(const ChunkLoad& load, int32_t num_sms, double* t_pipe, double* t_thr) {
   constexpr double kPipe = 64, kThroughputAlone = 95, kThroughputPaired = 116;
   constexpr double kShortPipe = 20, kShortThroughput = 25;
   const double longest = load.longest, total = (double)load.total, sms = num_sms;
   const double shorts = (double)load.short_units;
-  const double t_pipe = std::max(kPipe * longest, (kPipe * total + kShortPipe * shorts) / sms);
-  const double t_thr =
-      std::max(kThroughputAlone * longest,
-               (kThroughputPaired * total + kShortThroughput * shorts) /
-                   (kThroughputCtasPerSM * sms));
+  *t_pipe = std::max(kPipe * longest, (kPipe * total + kShortPipe * shorts) / sms);
+  *t_thr = std::max(kThroughputAlone * longest,
+                    (kThroughputPaired * total + kShortThroughput * shorts) /
+                        (kThroughputCtasPerSM * sms));
+}
+
+}  // namespace
+
+int plan_schedule(const ChunkLoad& load, int32_t num_sms) {
+  double t_pipe, t_thr;
+  schedule_estimates(load, num_sms, &t_pipe, &t_thr);
   return t_thr < t_pipe ? kChunkedThroughput : kChunkedPipelined;
+}
+
+double estimate_pass_us(const ChunkLoad& load, int32_t num_sms) {
+  double t_pipe, t_thr;
+  schedule_estimates(load, num_sms, &t_pipe, &t_thr);
+  return 0.1 * std::min(t_pipe, t_thr);  // tenths of a microsecond -> microseconds
+}
+
+int32_t choose_split_segment(const int32_t* cu, int32_t num_seqs, int32_t num_v_heads,
+                             int32_t num_sms) {
+  // a launch, the map composition and the state gather: small fixed costs per extra pass
+  constexpr double kSplitOverheadUs = 12.0;
+  int32_t longest = 0;
+  for (int32_t n = 0; n < num_seqs; ++n) longest = std::max(longest, cu[n + 1] - cu[n]);
+  double best = estimate_pass_us(chunk_load(cu, num_seqs, num_v_heads), num_sms);
+  int32_t best_seg = 0;
+  for (int32_t parts = 2; parts <= 16; ++parts) {
+    int32_t seg = (longest + parts - 1) / parts;
+    seg = (seg + 63) / 64 * 64;
+    if (seg < 64 || seg >= longest) continue;
+    // the virtual packs of the two passes, by length: pass A runs segment 0 of every prompt
+    // and two maps per middle segment of a split prompt; pass B the other segments
+    ChunkLoad a, b;
+    auto add = [](ChunkLoad& l, int32_t len, int32_t units) {
+      if (len <= 1) {
+        l.short_units += units;
+        return;
+      }
+      const int32_t c = (len + 63) / 64;
+      l.total += (int64_t)c * units;
+      l.longest = std::max(l.longest, c);
+    };
+    for (int32_t n = 0; n < num_seqs; ++n) {
+      const int32_t len = cu[n + 1] - cu[n];
+      add(a, std::min(len, seg), num_v_heads);
+      if (len <= seg) continue;
+      const int32_t np = (len + seg - 1) / seg;
+      for (int32_t q = 1; q + 1 < np; ++q) add(a, seg, 2 * num_v_heads);
+      for (int32_t q = 1; q < np; ++q) add(b, std::min(seg, len - q * seg), num_v_heads);
+    }
+    const double t = estimate_pass_us(a, num_sms) + estimate_pass_us(b, num_sms) +
+                     kSplitOverheadUs;
+    if (t < best) {
+      best = t;
+      best_seg = seg;
+    }
+  }
+  return best_seg;
 }
 
 namespace {

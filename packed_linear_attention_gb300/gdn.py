@@ -48,6 +48,7 @@ EXPORTS = (
     "gdn_chunked_schedule", "gdn_set_test_hook", "gdn_prefill_packed_pool",
     "gdn_prefill_launch_count", "gdn_prefill_packed_snapshot", "gdn_checkpoint_copy_event",
     "gdn_checkpoint_copy_join", "gdn_noalloc_read_status", "gdn_noalloc_set_test_hook",
+    "gdn_split_segment_auto",
 )
 
 
@@ -109,6 +110,7 @@ def load(path: str = LIB_PATH):
             "gdn_checkpoint_copy_event": (I32, [P, ctypes.POINTER(P)]),
             "gdn_checkpoint_copy_join": (I32, [P, P]),
             "gdn_noalloc_read_status": (I32, [IP, P]),
+            "gdn_split_segment_auto": (I32, [I32, IP, I32, I32, IP]),
             "gdn_noalloc_set_test_hook": (I32, [I32]),
             "gdn_prefill_split_workspace_size": (I32, [CFG, I32, IP, IP, IP, I32,
                                                        ctypes.POINTER(ctypes.c_size_t)]),
@@ -228,6 +230,15 @@ def gdn_chunked_schedule(cu_seqlens, num_v_heads: int, num_sms: int) -> int:
     out = ctypes.c_int32()
     _check(load().gdn_chunked_schedule(len(cu_seqlens) - 1, _i32(cu_seqlens), int(num_v_heads),
                                        int(num_sms), ctypes.byref(out)), "gdn_chunked_schedule")
+    return out.value
+
+
+def gdn_split_segment_auto(cu_seqlens, num_v_heads: int, num_sms: int) -> int:
+    """The segment length the cost model picks for gdn_prefill_packed_split (0: no split)."""
+    out = ctypes.c_int32()
+    _check(load().gdn_split_segment_auto(len(cu_seqlens) - 1, _i32(cu_seqlens),
+                                         int(num_v_heads), int(num_sms), ctypes.byref(out)),
+           "gdn_split_segment_auto")
     return out.value
 
 

@@ -222,6 +222,71 @@ def test_chunked_schedule_choice(lib):
         assert e.value.status == gdn.GDN_ERR_INVALID_ARGUMENT
 
 
+def _model_us(lens, hv, sms):
+    """The chunked cost model of gdn_chunked_schedule, written out: microseconds."""
+    lens = np.asarray(lens, np.int64)
+    ch = np.where(lens > 1, (lens + 63) // 64, 0)
+    W, L = float(ch.sum() * hv), float(ch.max()) if len(ch) else 0.0
+    S = float((lens <= 1).sum() * hv)
+    t_pipe = max(64 * L, (64 * W + 20 * S) / sms)
+    t_thr = max(95 * L, (116 * W + 25 * S) / (2 * sms))
+    return 0.1 * min(t_pipe, t_thr)
+
+
+def _split_choice(lens, hv, sms):
+    best, best_seg = _model_us(lens, hv, sms), 0
+    longest = max(lens)
+    for parts in range(2, 17):
+        seg = -(-longest // parts)
+        seg = -(-seg // 64) * 64
+        if seg < 64 or seg >= longest:
+            continue
+        a, a_hv, b = [], [], []
+        for n in lens:
+            a.append((min(n, seg), hv))
+            if n <= seg:
+                continue
+            np_ = -(-n // seg)
+            a += [(seg, 2 * hv)] * (np_ - 2)
+            b += [(min(seg, n - q * seg), hv) for q in range(1, np_)]
+
+        def us(items):
+            if not items:
+                return 0.0
+            lens_ = np.array([x for x, _ in items])
+            w = np.array([u for _, u in items], np.float64)
+            ch = np.where(lens_ > 1, (lens_ + 63) // 64, 0)
+            W, L, S = float((ch * w).sum()), float(ch.max()), float(((lens_ <= 1) * w).sum())
+            return 0.1 * min(max(64 * L, (64 * W + 20 * S) / sms),
+                             max(95 * L, (116 * W + 25 * S) / (2 * sms)))
+        t = us(a) + us(b) + 12.0
+        if t < best:
+            best, best_seg = t, seg
+    return best_seg
+
+
+def test_split_segment_choice(lib):
+    """The automatic segment length for sequence splitting against the cost model written
+    out here: no split for the wave or 4 x 8K (the SMs are full) nor for the ragged
+    prefix-cache pack (pass 1 alone would hold more work than the unsplit chain), a split
+    for one 32K prompt (its chain alone bounds it)."""
+    cu = lambda lens: np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    auto = gdn.gdn_split_segment_auto
+    assert auto(cu([1024] * 32), 32, 152) == 0
+    assert auto(cu([8192] * 4), 32, 152) == 0
+    one = auto(cu([32768]), 32, 152)
+    assert one > 0 and one % 64 == 0
+    r = I.ragged_prefix()
+    assert auto(r.cu_seqlens, 32, 152) == 0
+    rng = np.random.default_rng(5)
+    for _ in range(100):
+        lens = [int(x) for x in rng.integers(0, 20000, rng.integers(1, 12))]
+        hv, sms = int(rng.choice([4, 8, 32])), int(rng.choice([132, 152]))
+        assert auto(cu(lens), hv, sms) == _split_choice(lens, hv, sms), (lens, hv, sms)
+    with pytest.raises(gdn.GdnError):
+        auto(cu([5]), 0, 152)
+
+
 def test_test_hook_validation(lib):
     for hook in (0, 1):
         with pytest.raises(gdn.GdnError) as e:
