@@ -458,9 +458,15 @@ def run_secondary(torch, gdn, I, h, stream, flush, hbm_gbs):
     ms = _time_events(torch, lambda: gdn.prefill(h, buf, stream), stream, flush, steps=5)
     B = algorithmic_bytes(pack.total_tokens, 16, 32, 128, 1, pack.num_ckpts)
     entry = {"tokens": pack.total_tokens, "whole_us": ms * 1e3}
-    for parts in (3, 4):
-        seg = (pack.total_tokens + parts - 1) // parts  # rounded up to the chunk grid
-        seg = (seg + 63) // 64 * 64
+    auto_seg = gdn.gdn_split_segment_auto(pack.cu_seqlens, 32, sms)
+    for parts in (3, 4, "auto"):
+        if parts == "auto":
+            seg = auto_seg
+            if seg == 0:
+                continue
+        else:
+            seg = (pack.total_tokens + parts - 1) // parts  # rounded up to the chunk grid
+            seg = (seg + 63) // 64 * 64
         nbytes = gdn.gdn_prefill_split_workspace_size(buf.cfg, buf.cu, buf.ckpt_cu,
                                                       buf.ckpt_pos, seg)
         ws = torch.empty(nbytes, dtype=torch.uint8, device=buf.o.device)

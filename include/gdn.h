@@ -138,12 +138,13 @@ gdn_status gdn_set_test_hook(gdn_handle* handle, int32_t hook);
  * prompts (cu_seqlens_host: prefix sums, as for gdn_prefill_packed) with `num_v_heads`
  * value heads on a GPU with `num_sms` SMs: *schedule = 2 (pipelined) or 3 (throughput),
  * the gdn_set_kernel_preference codes. The choice is the smaller of two estimates from
- * costs measured on GB300 (6.4 us per chunk for a pipelined unit on its own SM, 9.5 us for
- * a throughput unit alone on its SM, 11.6 us for one of two sharing an SM; 2.0 and 2.5 us
- * per unit of a prompt with one token or none, which the same launch runs with the decode
- * step's arithmetic), over W = the chunks of all other (prompt, value head) units, Lmax =
- * the chunks of the longest and S = the short units:
- *   pipelined:  max(6.4 Lmax, (6.4 W + 2.0 S) / num_sms)
+ * costs measured on GB300 (6.4 us per chunk for a pipelined unit on its own SM, plus two
+ * chunks of pipeline fill and drain per unit; 9.5 us for a throughput unit alone on its SM,
+ * 11.6 us for one of two sharing an SM; 2.0 and 2.5 us per unit of a prompt with one token
+ * or none, which the same launch runs with the decode step's arithmetic), over W = the
+ * chunks of the U other (prompt, value head) units, Lmax = the chunks of the longest and
+ * S = the short units:
+ *   pipelined:  max(6.4 (Lmax + 2), (6.4 (W + 2 U) + 2.0 S) / num_sms)
  *   throughput: max(9.5 Lmax, (11.6 W + 2.5 S) / (2 num_sms)).
  * Both schedules give bit-identical results; only the time differs. Host-only arithmetic,
  * no CUDA call. Errors: INVALID_ARGUMENT (num_seqs < 0, cu NULL with num_seqs > 0,

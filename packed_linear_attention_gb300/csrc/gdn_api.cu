@@ -949,6 +949,7 @@ gdn::ChunkLoad vseq_load(const std::vector<VSeq>& vs, int32_t units_per_prompt) 
     }
     const int32_t c = (x.len + 63) / 64;
     l.total += (int64_t)c * units_per_prompt;
+    l.units += units_per_prompt;
     l.longest = std::max(l.longest, c);
   }
   return l;

@@ -142,6 +142,7 @@ struct ChunkLoad {
   int64_t total = 0;
   int32_t longest = 0;
   int64_t short_units = 0;
+  int64_t units = 0;  // units with at least one chunk
 };
 // The load of a pack of prompts (cu: host prefix sums) with `units_per_prompt` units each.
 inline ChunkLoad chunk_load(const int32_t* cu, int32_t num_seqs, int32_t units_per_prompt) {
@@ -154,6 +155,7 @@ inline ChunkLoad chunk_load(const int32_t* cu, int32_t num_seqs, int32_t units_p
     }
     const int32_t c = (len + 63) / 64;
     l.total += (int64_t)c * units_per_prompt;
+    l.units += units_per_prompt;
     if (c > l.longest) l.longest = c;
   }
   return l;

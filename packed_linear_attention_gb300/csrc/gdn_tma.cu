@@ -84,16 +84,20 @@ bool make_qkv_maps(const PrefillArgs& a, int64_t total_tokens, int head_dim, CUt
 // 1,024-token unit, a pipelined unit on its own SM, a throughput CTA alone on its SM and a
 // throughput CTA sharing its SM with a second one; per unit of a prompt with one token or
 // none (the state read and written once by a whole CTA), on a pipelined or throughput CTA
-// slot. A pack takes at least its longest unit's chain and at least its total work spread
-// over the SMs' slots.
+// slot. A pipelined unit also costs two chunks of fill and drain (its chain group starts
+// one chunk behind the prep group, and both run each unit's first and last chunk alone),
+// which decides packs of short prompts. A pack takes at least its longest unit's chain and
+// at least its total work spread over the SMs' slots.
 namespace {
 
 void schedule_estimates(const ChunkLoad& load, int32_t num_sms, double* t_pipe, double* t_thr) {
   constexpr double kPipe = 64, kThroughputAlone = 95, kThroughputPaired = 116;
   constexpr double kShortPipe = 20, kShortThroughput = 25;
+  constexpr double kPipeFill = 2;  // chunks per pipelined unit
   const double longest = load.longest, total = (double)load.total, sms = num_sms;
-  const double shorts = (double)load.short_units;
-  *t_pipe = std::max(kPipe * longest, (kPipe * total + kShortPipe * shorts) / sms);
+  const double shorts = (double)load.short_units, units = (double)load.units;
+  *t_pipe = std::max(kPipe * (longest + (units > 0 ? kPipeFill : 0)),
+                     (kPipe * (total + kPipeFill * units) + kShortPipe * shorts) / sms);
   *t_thr = std::max(kThroughputAlone * longest,
                     (kThroughputPaired * total + kShortThroughput * shorts) /
                         (kThroughputCtasPerSM * sms));
@@ -135,6 +139,7 @@ int32_t choose_split_segment(const int32_t* cu, int32_t num_seqs, int32_t num_v_
       }
       const int32_t c = (len + 63) / 64;
       l.total += (int64_t)c * units;
+      l.units += units;
       l.longest = std::max(l.longest, c);
     };
     for (int32_t n = 0; n < num_seqs; ++n) {

@@ -211,8 +211,8 @@ def test_chunked_schedule_choice(lib):
         hv, sms = int(rng.choice([4, 8, 32, 64])), int(rng.choice([1, 132, 152]))
         ch = np.where(lens > 1, (lens + 63) // 64, 0)  # prompts of <= 1 token: short units
         W, L = float(ch.sum() * hv), float(ch.max())
-        S = float((lens <= 1).sum() * hv)
-        t_pipe = max(64 * L, (64 * W + 20 * S) / sms)
+        S, U = float((lens <= 1).sum() * hv), float((lens > 1).sum() * hv)
+        t_pipe = max(64 * (L + (2 if U else 0)), (64 * (W + 2 * U) + 20 * S) / sms)
         t_thr = max(95 * L, (116 * W + 25 * S) / (2 * sms))
         assert choose(cu(lens), hv, sms) == (thr if t_thr < t_pipe else pipe)
     for bad in ((cu([3]), 0, 152), (cu([3]), 8, 0), (np.array([1, 4], np.int32), 8, 152),
@@ -227,8 +227,8 @@ def _model_us(lens, hv, sms):
     lens = np.asarray(lens, np.int64)
     ch = np.where(lens > 1, (lens + 63) // 64, 0)
     W, L = float(ch.sum() * hv), float(ch.max()) if len(ch) else 0.0
-    S = float((lens <= 1).sum() * hv)
-    t_pipe = max(64 * L, (64 * W + 20 * S) / sms)
+    S, U = float((lens <= 1).sum() * hv), float((lens > 1).sum() * hv)
+    t_pipe = max(64 * (L + (2 if U else 0)), (64 * (W + 2 * U) + 20 * S) / sms)
     t_thr = max(95 * L, (116 * W + 25 * S) / (2 * sms))
     return 0.1 * min(t_pipe, t_thr)
 
@@ -257,7 +257,8 @@ def _split_choice(lens, hv, sms):
             w = np.array([u for _, u in items], np.float64)
             ch = np.where(lens_ > 1, (lens_ + 63) // 64, 0)
             W, L, S = float((ch * w).sum()), float(ch.max()), float(((lens_ <= 1) * w).sum())
-            return 0.1 * min(max(64 * L, (64 * W + 20 * S) / sms),
+            U = float(((lens_ > 1) * w).sum())
+            return 0.1 * min(max(64 * (L + (2 if U else 0)), (64 * (W + 2 * U) + 20 * S) / sms),
                              max(95 * L, (116 * W + 25 * S) / (2 * sms)))
         t = us(a) + us(b) + 12.0
         if t < best:

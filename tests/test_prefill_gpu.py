@@ -317,7 +317,7 @@ def test_auto_pack_vs_alone_bitwise_across_schedules():
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     n_prompts = (6 * sms + 31) // 32
     rng = np.random.default_rng(34)
-    lengths = [int(x) for x in rng.integers(1, 200, n_prompts)]
+    lengths = [int(x) for x in rng.integers(1000, 2000, n_prompts)]
     ck = [[q for q in range(64, n + 1, 64)] + ([n] if n % 64 else []) for n in lengths]
     p = I.make_pack(lengths, num_k_heads=16, num_v_heads=32, head_dim=128, io_dtype="bf16",
                     seed=35, init_std=0.02, ckpt_lists=ck)
