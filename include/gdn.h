@@ -138,14 +138,22 @@ gdn_status gdn_set_test_hook(gdn_handle* handle, int32_t hook);
  * prompts (cu_seqlens_host: prefix sums, as for gdn_prefill_packed) with `num_v_heads`
  * value heads on a GPU with `num_sms` SMs: *schedule = 2 (pipelined) or 3 (throughput),
  * the gdn_set_kernel_preference codes. The choice is the smaller of two estimates from
- * costs measured on GB300 (6.4 us per chunk for a pipelined unit on its own SM, plus two
- * chunks of pipeline fill and drain per unit; 9.5 us for a throughput unit alone on its SM,
- * 11.6 us for one of two sharing an SM; 2.0 and 2.5 us per unit of a prompt with one token
- * or none, which the same launch runs with the decode step's arithmetic), over W = the
- * chunks of the U other (prompt, value head) units, Lmax = the chunks of the longest and
- * S = the short units:
- *   pipelined:  max(6.4 (Lmax + 2), (6.4 (W + 2 U) + 2.0 S) / num_sms)
- *   throughput: max(9.5 Lmax, (11.6 W + 2.5 S) / (2 num_sms)).
+ * costs measured on GB300 (microseconds): 5.12 per chunk plus 15.7 per unit for a
+ * pipelined unit on its own SM; 8.93 per chunk plus 13.2 per unit for one of two
+ * throughput units sharing an SM, 6.38 plus 17.3 for one alone; 8.0 and 16.6 per unit of a
+ * prompt with one token or none (which the same launch runs with the decode step's
+ * arithmetic) on a pipelined or throughput slot. Over W = the chunks of the U other
+ * (prompt, value head) units, Lmax = the chunks of the longest and S = the short units:
+ *   pipelined:  max(5.12 Lmax + 15.7, (5.12 W + 15.7 U + 8.0 S) / num_sms,
+ *                   ceil(U / num_sms) (5.12 W / U + 15.7))
+ *   throughput: max(Lchain, R, (8.93 W + 13.2 U + 16.6 S) / (2 num_sms)), with
+ *               Lchain = 8.93 Lmax + 13.2 when U > num_sms, else 6.38 Lmax + 17.3, and
+ *               R = F (8.93 W / U + 13.2) + the last round, F = floor(U / (2 num_sms)):
+ *               paired (8.93 W / U + 13.2) if its units outnumber the SMs, else alone
+ *               (6.38 W / U + 17.3), else nothing
+ * (the 15.7 and 17.3 terms and the rounds only when U > 0): a unit never moves between
+ * SMs, so a pack runs in whole rounds, and a throughput pack with more units than SMs
+ * has SMs running two units at once.
  * Both schedules give bit-identical results; only the time differs. Host-only arithmetic,
  * no CUDA call. Errors: INVALID_ARGUMENT (num_seqs < 0, cu NULL with num_seqs > 0,
  * cu[0] != 0 or decreasing, num_v_heads < 1, num_sms < 1, schedule NULL). */

@@ -9,10 +9,12 @@
 // segments once more from their true initial states.
 //
 //  * fill_states: the initial states of a pass (copies of the caller's, zeros, identities);
-//  * compose_maps: per (split prompt, value head), S_start(p+1) = S_start(p) M_p + B_p in
-//    fp32, in segment order;
+//  * compose_maps: per (split prompt, value head, block of rows),
+//    S_start(p+1) = S_start(p) M_p + B_p in fp32, in segment order;
 //  * gather_states: final states from the passes' scratch into the caller's array.
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "gdn_internal.h"
 
@@ -38,57 +40,72 @@ __global__ void __launch_bounds__(kThreads) fill_states_kernel(float* dst, const
   }
 }
 
-// One block per (split prompt, value head); S and the current M in shared memory (fp32,
-// 2 D x D). Thread t owns row t / (256 / D) and D^2 / 256 consecutive columns of S M.
+// Rows of S M + B depend only on the same rows of S, so one block owns kRows rows of S for
+// one (split prompt, value head): grid = jobs x heads x D / kRows. Shared memory holds the
+// block's rows of S and the whole current M (fp32). Thread t owns kRpt rows and the 4
+// columns 4 (t mod D/4) .. +3: at D = 128 a warp reads one S entry (broadcast) and 512
+// contiguous bytes of an M row per k. Each entry sums its products from zero in k order
+// and then adds B's.
+constexpr int kRows = 16;
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) compose_maps_kernel(const SplitCompose* jobs,
                                                                 const float* finals_a,
                                                                 float* inits_c, int hv) {
-  constexpr int kPerRow = kThreads / D, kCols = D / kPerRow;
+  constexpr int kGroups = D / 4, kRpt = kRows * kGroups / kThreads;
+  constexpr int kBlocks = D / kRows;
   extern __shared__ float4 smem4[];
-  float* S = reinterpret_cast<float*>(smem4);  // [D][D]
-  float* M = S + D * D;                          // [D][D]
-  const SplitCompose job = jobs[blockIdx.x / hv];
-  const int h = blockIdx.x % hv;
+  float* M = reinterpret_cast<float*>(smem4);  // [D][D]
+  float* S = M + D * D;                          // [kRows][D]
+  const int per_job = hv * kBlocks;
+  const SplitCompose job = jobs[blockIdx.x / per_job];
+  const int h = (blockIdx.x % per_job) / kBlocks, row0 = (blockIdx.x % kBlocks) * kRows;
   const size_t per = (size_t)D * D;
-  const int tid = threadIdx.x, r = tid / kPerRow, c0 = kCols * (tid % kPerRow);
+  const int tid = threadIdx.x, cg = tid % kGroups, rg = tid / kGroups;
   auto state = [&](const float* base, int i) { return base + ((size_t)i * hv + h) * per; };
-  auto state_mut = [&](float* base, int i) { return base + ((size_t)i * hv + h) * per; };
+  auto rows = [&](int i) { return row0 * D + i; };  // offset of this block's rows
 
-  // S = final state of segment 0 (run from the caller's initial state)
-  const float4* s0 = reinterpret_cast<const float4*>(state(finals_a, job.first_final));
-  for (int e = tid; e < D * D / 4; e += kThreads) reinterpret_cast<float4*>(S)[e] = s0[e];
+  // S = final state of segment 0 (run from the caller's initial state), this block's rows
+  const float4* s0 = reinterpret_cast<const float4*>(state(finals_a, job.first_final) + rows(0));
+  for (int e = tid; e < kRows * D / 4; e += kThreads) reinterpret_cast<float4*>(S)[e] = s0[e];
   __syncthreads();
   for (int p = 1; p < job.num_segments; ++p) {
     // initial state of segment p
-    float4* dst = reinterpret_cast<float4*>(state_mut(inits_c, job.first_init + p - 1));
-    for (int e = tid; e < D * D / 4; e += kThreads)
+    float4* dst = reinterpret_cast<float4*>(
+        const_cast<float*>(state(inits_c, job.first_init + p - 1)) + rows(0));
+    for (int e = tid; e < kRows * D / 4; e += kThreads)
       dst[e] = reinterpret_cast<const float4*>(S)[e];
     if (p + 1 == job.num_segments) break;
     // S <- S M_p + B_p (B_p at first_map + 2 (p - 1), M_p right after it)
     const float4* m =
         reinterpret_cast<const float4*>(state(finals_a, job.first_map + 2 * p - 1));
-    for (int e = tid; e < D * D / 4; e += kThreads) reinterpret_cast<float4*>(M)[e] = m[e];
+    for (int e = tid; e < D * D / 4; e += kThreads) smem4[e] = m[e];
+    const float* b = state(finals_a, job.first_map + 2 * p - 2) + rows(0);
+    float4 acc[kRpt], bv[kRpt];
+#pragma unroll
+    for (int i = 0; i < kRpt; ++i) {
+      bv[i] = reinterpret_cast<const float4*>(b + (rg * kRpt + i) * D)[cg];
+      acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     __syncthreads();
-    float acc[kCols];
-#pragma unroll
-    for (int j = 0; j < kCols; ++j) acc[j] = 0.f;
+#pragma unroll 4
     for (int k = 0; k < D; ++k) {
-      const float s = S[r * D + k];
-      const float4* mrow = reinterpret_cast<const float4*>(M + k * D + c0);
+      const float4 x = reinterpret_cast<const float4*>(M + k * D)[cg];
 #pragma unroll
-      for (int j = 0; j < kCols / 4; ++j) {
-        const float4 x = mrow[j];
-        acc[4 * j] += s * x.x;
-        acc[4 * j + 1] += s * x.y;
-        acc[4 * j + 2] += s * x.z;
-        acc[4 * j + 3] += s * x.w;
+      for (int i = 0; i < kRpt; ++i) {
+        const float sv = S[(rg * kRpt + i) * D + k];
+        acc[i].x += sv * x.x;
+        acc[i].y += sv * x.y;
+        acc[i].z += sv * x.z;
+        acc[i].w += sv * x.w;
       }
     }
-    const float* b = state(finals_a, job.first_map + 2 * p - 2) + (size_t)r * D + c0;
     __syncthreads();  // every read of S and M done
 #pragma unroll
-    for (int j = 0; j < kCols; ++j) S[r * D + c0 + j] = acc[j] + b[j];
+    for (int i = 0; i < kRpt; ++i)
+      reinterpret_cast<float4*>(S + (rg * kRpt + i) * D)[cg] =
+          make_float4(acc[i].x + bv[i].x, acc[i].y + bv[i].y, acc[i].z + bv[i].z,
+                      acc[i].w + bv[i].w);
     __syncthreads();
   }
 }
@@ -121,20 +138,19 @@ int launch_compose_maps(const SplitCompose* jobs, int num_jobs, const float* fin
                         float* inits_c, int hv, int d, void* stream) {
   if (num_jobs == 0) return 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int smem = 2 * d * d * (int)sizeof(float);
+  const int smem = (d * d + kRows * d) * (int)sizeof(float);
+  const unsigned grid = (unsigned)(num_jobs * hv * (d / kRows));
   if (d == 128) {
-    static bool configured = false;
-    if (!configured) {
-      const cudaError_t e = cudaFuncSetAttribute(
-          compose_maps_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return (int)e;
-      configured = true;
-    }
-    compose_maps_kernel<128><<<num_jobs * hv, kThreads, smem, st>>>(jobs, finals_a, inits_c,
-                                                                    hv);
+    static std::once_flag once;
+    static cudaError_t configured = cudaSuccess;
+    std::call_once(once, [smem] {
+      configured = cudaFuncSetAttribute(compose_maps_kernel<128>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    });
+    if (configured != cudaSuccess) return (int)configured;
+    compose_maps_kernel<128><<<grid, kThreads, smem, st>>>(jobs, finals_a, inits_c, hv);
   } else if (d == 64) {
-    compose_maps_kernel<64><<<num_jobs * hv, kThreads, smem, st>>>(jobs, finals_a, inits_c,
-                                                                   hv);
+    compose_maps_kernel<64><<<grid, kThreads, smem, st>>>(jobs, finals_a, inits_c, hv);
   } else {
     return (int)cudaErrorInvalidValue;
   }

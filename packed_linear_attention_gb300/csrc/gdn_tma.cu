@@ -8,6 +8,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -80,27 +81,41 @@ bool make_qkv_maps(const PrefillArgs& a, int64_t total_tokens, int head_dim, CUt
          make_bf16_map(tv, a.v, (uint64_t)a.hv_heads * head_dim, rows);
 }
 
-// Estimated times from costs measured on GB300 (tenths of a microsecond): per chunk of a
-// 1,024-token unit, a pipelined unit on its own SM, a throughput CTA alone on its SM and a
-// throughput CTA sharing its SM with a second one; per unit of a prompt with one token or
-// none (the state read and written once by a whole CTA), on a pipelined or throughput CTA
-// slot. A pipelined unit also costs two chunks of fill and drain (its chain group starts
-// one chunk behind the prep group, and both run each unit's first and last chunk alone),
-// which decides packs of short prompts. A pack takes at least its longest unit's chain and
-// at least its total work spread over the SMs' slots.
+// Estimated times (microseconds) from costs measured on GB300 with uniform packs of 2- to
+// 64-chunk units (8 value heads, L2 flushed, the current kernels):
+//  * pipelined (one unit per SM): 5.12 per chunk plus 15.7 per unit (the pipeline's fill and
+//    drain and the unit's set-up);
+//  * throughput, two units per SM: 8.93 per chunk plus 13.2 per unit; a unit alone on its
+//    SM: 6.38 per chunk plus 17.3;
+//  * a unit of a prompt with one token or none: 8.0 per pipelined slot, 16.6 per
+//    throughput slot.
+// A pack takes at least its longest unit's chain, at least its total work spread over the
+// SMs' slots, and, since a unit never moves between SMs, at least its whole rounds of the
+// mean unit: ceil(units / SMs) pipelined rounds; in the throughput schedule one paired
+// round per 2 x SMs units, then a last round that is paired when its units outnumber the
+// SMs and alone otherwise. Once units outnumber SMs the longest unit runs paired too.
 namespace {
 
 void schedule_estimates(const ChunkLoad& load, int32_t num_sms, double* t_pipe, double* t_thr) {
-  constexpr double kPipe = 64, kThroughputAlone = 95, kThroughputPaired = 116;
-  constexpr double kShortPipe = 20, kShortThroughput = 25;
-  constexpr double kPipeFill = 2;  // chunks per pipelined unit
+  constexpr double kPipeChunk = 5.12, kPipeUnit = 15.7, kPipeShort = 8.0;
+  constexpr double kThrChunk = 8.93, kThrUnit = 13.2, kThrShort = 16.6;
+  constexpr double kAloneChunk = 6.38, kAloneUnit = 17.3;
   const double longest = load.longest, total = (double)load.total, sms = num_sms;
   const double shorts = (double)load.short_units, units = (double)load.units;
-  *t_pipe = std::max(kPipe * (longest + (units > 0 ? kPipeFill : 0)),
-                     (kPipe * (total + kPipeFill * units) + kShortPipe * shorts) / sms);
-  *t_thr = std::max(kThroughputAlone * longest,
-                    (kThroughputPaired * total + kShortThroughput * shorts) /
-                        (kThroughputCtasPerSM * sms));
+  const double has = units > 0 ? 1.0 : 0.0;
+  const double mean = units > 0 ? total / units : 0.0;
+  const double rounds = std::ceil(units / sms);
+  *t_pipe = std::max({longest * kPipeChunk + has * kPipeUnit,
+                      (total * kPipeChunk + units * kPipeUnit + shorts * kPipeShort) / sms,
+                      rounds * (mean * kPipeChunk + kPipeUnit)});
+  const double chain = units > sms ? longest * kThrChunk + kThrUnit
+                                   : longest * kAloneChunk + has * kAloneUnit;
+  const double slots = kThroughputCtasPerSM * sms;
+  const double full = std::floor(units / slots), last = units - full * slots;
+  const double paired = mean * kThrChunk + kThrUnit, alone = mean * kAloneChunk + kAloneUnit;
+  const double thr_rounds = full * paired + (last > sms ? paired : last > 0 ? alone : 0.0);
+  *t_thr = std::max({chain, thr_rounds,
+                     (total * kThrChunk + units * kThrUnit + shorts * kThrShort) / slots});
 }
 
 }  // namespace
@@ -114,7 +129,7 @@ int plan_schedule(const ChunkLoad& load, int32_t num_sms) {
 double estimate_pass_us(const ChunkLoad& load, int32_t num_sms) {
   double t_pipe, t_thr;
   schedule_estimates(load, num_sms, &t_pipe, &t_thr);
-  return 0.1 * std::min(t_pipe, t_thr);  // tenths of a microsecond -> microseconds
+  return std::min(t_pipe, t_thr);
 }
 
 int32_t choose_split_segment(const int32_t* cu, int32_t num_seqs, int32_t num_v_heads,
