@@ -104,6 +104,26 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t& phase, bool& p
   return !__syncthreads_or(!ok);
 }
 
+// wait_all for the q/k copy and (when `with_v`) the v copy, with one block barrier.
+__device__ __forceinline__ bool wait_copies(uint64_t* bar_kq, uint32_t& ph_kq, bool& kq_pending,
+                                            uint64_t* bar_v, uint32_t& ph_v, bool& v_pending,
+                                            bool with_v) {
+  bool ok = mbar_wait_bounded(bar_kq, ph_kq & 1u, kWaitLimit);
+  if (ok) {
+    ph_kq ^= 1u;
+    kq_pending = false;
+  }
+  if (ok && with_v) {
+    ok = mbar_wait_bounded(bar_v, ph_v & 1u, kWaitLimit);
+    if (ok) {
+      ph_v ^= 1u;
+      v_pending = false;
+    }
+  }
+  tc_fence_after();
+  return !__syncthreads_or(!ok);
+}
+
 // Makes generic-proxy smem writes and TMEM stores visible to the next MMA issue.
 __device__ __forceinline__ void publish_operands() {
   fence_proxy_async_smem();
@@ -378,10 +398,8 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
     const int L = min(kC, sd.len - t0);
 
     // ---- (2) wait for q, k, v; convert in place to fp16 (q, k normalised); zero past L ----
-    if (!(ok = wait_all(&sm.bar_kq, ph_kq, kq_inflight))) break;
-    if (!vz) {
-      if (!(ok = wait_all(&sm.bar_v, ph_v, v_inflight))) break;
-    }
+    if (!(ok = wait_copies(&sm.bar_kq, ph_kq, kq_inflight, &sm.bar_v, ph_v, v_inflight, !vz)))
+      break;
     if (tid == 0 && c + 1 < nchunks) {  // warm L2 with the next chunk's q, k, v
       const int nrow = sd.tok_start + t0 + kC;
 #pragma unroll
@@ -510,10 +528,23 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
     if (!(ok = wait_all(&sm.bar_mma, ph_mma, mma_inflight))) break;
 
     // ---- (7) W^T -> smem (fp16, MN-major B: rows d_k, columns tokens) ---------------------------
+    // Once every warp has read W^T out of R0, the first half of M3 (V^T T2^T, whose operands
+    // were published before M2) starts into R0 while the warps store W^T.
     {
       uint32_t r[32];
       tmem_ld32(t_lane + TM_R0 + 32 * half, r);
       tmem_ld_wait();
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (tid == 0) {
+        const uint32_t id_u = idesc_f16(128, 64, 1, 0);
+        const uint32_t v0 = smem_u32(sV), t2 = smem_u32(sT2);
+#pragma unroll
+        for (int s = 0; s < kC / 16; ++s)
+          mma_f16_ss(tbase + TM_R0, smem_desc_sw128(v0 + s * 2048, 8192, 1024),
+                     smem_desc_sw128(t2 + s * 32, 16, 1024), id_u, s > 0);
+      }
 #pragma unroll
       for (int e = 0; e < 32; e += 8) {
         float x[8];
@@ -524,15 +555,10 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
     }
     publish_operands();
 
-    // ---- (8) M3: D^T = V^T T2^T - S16 W^T -> R0 ------------------------------------------------
+    // ---- (8) M3: D^T = V^T T2^T - S16 W^T -> R0 (V^T T2^T already issued) ---------------------
     if (tid == 0) {
-      const uint32_t id_u = idesc_f16(128, 64, 1, 0);
       const uint32_t id_w = idesc_f16(128, 64, 0, 1, 0, 1);  // B negated
-      const uint32_t v0 = smem_u32(sV), t2 = smem_u32(sT2), w0 = smem_u32(sWD);
-#pragma unroll
-      for (int s = 0; s < kC / 16; ++s)
-        mma_f16_ss(tbase + TM_R0, smem_desc_sw128(v0 + s * 2048, 8192, 1024),
-                   smem_desc_sw128(t2 + s * 32, 16, 1024), id_u, s > 0);
+      const uint32_t w0 = smem_u32(sWD);
 #pragma unroll
       for (int s = 0; s < kD / 16; ++s)
         mma_f16_ts(tbase + TM_R0, tbase + TM_S16 + s * 8,
@@ -549,10 +575,25 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
     }
 
     // ---- (9) D^T and D'^T = D^T diag(e^{G_L - G}) -> smem (fp16 K-major A operands) -------------
+    // Once every warp has read D^T out of R0, the first half of M4 (S16 Q~^T; Q~ was published
+    // before M2) starts into R0 while the warps store D and D'.
     {
       uint32_t r[32];
       tmem_ld32(t_lane + TM_R0 + 32 * half, r);
       tmem_ld_wait();
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (tid == 0) {
+        const uint32_t id_n64 = idesc_f16(128, 64, 0, 0);
+        const uint32_t kq = smem_u32(sKQ);
+#pragma unroll
+        for (int s = 0; s < kD / 16; ++s) {
+          const uint32_t off = 8192 + (s >> 2) * 16384 + (s & 3) * 32;  // Q~ rows 64-127
+          mma_f16_ts(tbase + TM_R0, tbase + TM_S16 + s * 8, smem_desc_sw128(kq + off, 16, 1024),
+                     id_n64, s > 0);
+        }
+      }
 #pragma unroll
       for (int e = 0; e < 32; e += 8) {
         const float4 da = *reinterpret_cast<const float4*>(sDec + 32 * half + e);
@@ -573,16 +614,10 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
     }
     publish_operands();
 
-    // ---- (10) O^T = S16 Q~^T + D^T P^T -> R0;  S32 += D'^T K ----------------------------------
+    // ---- (10) O^T = S16 Q~^T + D^T P^T -> R0 (S16 Q~^T already issued);  S32 += D'^T K ------
     if (tid == 0) {
       const uint32_t id_n64 = idesc_f16(128, 64, 0, 0);
       const uint32_t kq = smem_u32(sKQ), d0 = smem_u32(sWD), p0 = smem_u32(sP);
-#pragma unroll
-      for (int s = 0; s < kD / 16; ++s) {
-        const uint32_t off = 8192 + (s >> 2) * 16384 + (s & 3) * 32;  // Q~ rows 64-127
-        mma_f16_ts(tbase + TM_R0, tbase + TM_S16 + s * 8, smem_desc_sw128(kq + off, 16, 1024),
-                   id_n64, s > 0);
-      }
 #pragma unroll
       for (int s = 0; s < kC / 16; ++s)
         mma_f16_ss(tbase + TM_R0, smem_desc_sw128(d0 + s * 32, 16, 1024),
