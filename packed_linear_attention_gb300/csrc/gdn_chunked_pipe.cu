@@ -839,16 +839,17 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
 
 int launch_chunked_pipelined(const PrefillArgs& a, int64_t total_tokens, void* stream) {
   if (a.num_units == 0) return 0;
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<int> configured[kMaxDevices];
+  const int ce = configure_once(configured, [] {
     for (const void* k : {(const void*)chunked_pipe_kernel<128>,
                           (const void*)chunked_pipe_kernel<64>}) {
-      cudaError_t e =
+      const cudaError_t e =
           cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
       if (e != cudaSuccess) return (int)e;
     }
-    configured = true;
-  }
+    return 0;
+  });
+  if (ce != 0) return ce;
   ChunkedParams P;
   P.a = a;
   if (!make_qkv_maps(a, total_tokens, a.head_dim, &P.tq, &P.tk, &P.tv) ||

@@ -10,7 +10,9 @@
 // hands out blocks roughly in index order, runs a longest-processing-time-first schedule.
 #pragma once
 #include <cuda.h>
+#include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -214,5 +216,21 @@ void write_worklist(void* dst, const PrefillPlan& plan, const gdn_config* cfg, i
 // Row block of a unit for each kernel family.
 constexpr int kRecurrentRows = 32;
 constexpr bool kChunkedReady = true;
+
+// Once-per-device kernel set-up (cudaFuncSetAttribute acts on the current device): runs
+// `fn` on the first call for each device and remembers success. Concurrent first calls
+// may each run it, so `fn` must be idempotent. Returns fn's error, or a runtime error.
+constexpr int kMaxDevices = 64;
+template <class F>
+int configure_once(std::atomic<int> (&done)[kMaxDevices], F fn) {
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return (int)e;
+  const bool tracked = dev >= 0 && dev < kMaxDevices;
+  if (tracked && done[dev].load(std::memory_order_acquire)) return 0;
+  const int r = fn();
+  if (r == 0 && tracked) done[dev].store(1, std::memory_order_release);
+  return r;
+}
 
 }  // namespace gdn

@@ -34,7 +34,7 @@
 
 namespace {
 
-constexpr int kMaxDevices = 64;
+using gdn::kMaxDevices;
 
 // The scratch every call on this device shares (work list + status word).
 static __device__ __align__(256) uint8_t g_noalloc_scratch[GDN_NOALLOC_SCRATCH_BYTES];

@@ -14,8 +14,6 @@
 //  * gather_states: final states from the passes' scratch into the caller's array.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "gdn_internal.h"
 
 namespace gdn {
@@ -141,13 +139,12 @@ int launch_compose_maps(const SplitCompose* jobs, int num_jobs, const float* fin
   const int smem = (d * d + kRows * d) * (int)sizeof(float);
   const unsigned grid = (unsigned)(num_jobs * hv * (d / kRows));
   if (d == 128) {
-    static std::once_flag once;
-    static cudaError_t configured = cudaSuccess;
-    std::call_once(once, [smem] {
-      configured = cudaFuncSetAttribute(compose_maps_kernel<128>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static std::atomic<int> configured[kMaxDevices];
+    const int ce = configure_once(configured, [smem] {
+      return (int)cudaFuncSetAttribute(compose_maps_kernel<128>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
-    if (configured != cudaSuccess) return (int)configured;
+    if (ce != 0) return ce;
     compose_maps_kernel<128><<<grid, kThreads, smem, st>>>(jobs, finals_a, inits_c, hv);
   } else if (d == 64) {
     compose_maps_kernel<64><<<grid, kThreads, smem, st>>>(jobs, finals_a, inits_c, hv);
