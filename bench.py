@@ -56,25 +56,27 @@ def algorithmic_flops(T, Hk, Hv, d, C=64):
     return T * Hv * (6 * d * d + 6 * C * d) + T * Hk * (4 * C * d)
 
 
-# DRAM traffic of the prefill kernel per full-wave launch, from an ncu capture of this
-# workload (dram__bytes_read.sum + dram__bytes_write.sum; a one-pass metric, so captured
-# at full size: `ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,
-# dram__bytes_write.sum --clock-control none python bench.py --steps 3 --warmup 3
-# --no-cpu-baseline --no-e2e`). It is reported only while the kernel sources hash to
-# the values it was measured on; any change to them reports null until re-measured.
+# DRAM traffic of the prefill kernel per full-wave launch (the median of three launches),
+# from an ncu capture of this workload (dram__bytes_read.sum + dram__bytes_write.sum; one
+# pass on the 8-prompt case, so captured at full size: `ncu --metrics
+# gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum --clock-control none
+# -k regex:chunked_prefill -s 3 -c 3 python bench.py --steps 3 --warmup 3
+# --no-cpu-baseline --no-e2e --no-secondary`). It is reported only while the kernel
+# sources hash to the values it was measured on; any change to them reports null until
+# re-measured.
 MEASURED_TRAFFIC = {
     "sources": {
         "packed_linear_attention_gb300/csrc/gdn_chunked.cu":
-            "617fcc340d2cace43f6a164452edf5eb1569a5ce419ee7af548ad0e5791ac66b",
+            "35a04f234522e002070463dea90d68f2a00e531eea85fee8a7bda5f3206c372a",
         "packed_linear_attention_gb300/csrc/gdn_chunk_util.cuh":
-            "31ea72c253f10039cbce7a7b89024ca5afc4fd8a37a8938cb481b82c221d4590",
+            "92633a3576a4cac7806eace0e638f52b98ad447f585909d4c542593632791654",
         "packed_linear_attention_gb300/csrc/ptx_sm103.cuh":
-            "7656f71f13ce2d5d3e3fa32de31a5fce86755fc036450c47a26a30d1a01c6b56",
+            "762c9e7ef68fa3e883aaeb592d47ce09eed2b387cc7b6e46fa74fa53d9b1da60",
         "packed_linear_attention_gb300/csrc/gdn_tma.cu":
-            "0336c41ea051cad488f5d43c034eb75bee8fb8e3fc662d50a87f672d267ebdcb",
+            "b97a465a15c3850359ec63c6925ea5d4f1962a058db1f247ccd5c0a9055e72f2",
     },
     "read_bytes": 546.0e6,
-    "write_bytes": 357.0e6,
+    "write_bytes": 357.1e6,
 }
 
 
