@@ -391,6 +391,9 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
   bool v_inflight = nchunks > 0 && !vz, mma_inflight = false;
   bool store_pending = false;  // a TMA store of output rows still reading the staging tile
   int c_next = sd.ckpt_begin;
+  // the next checkpoint's position (-1: none left), read again only after a checkpoint is
+  // stored, so that no chunk waits on a global load to decide
+  int ck_pos = c_next < sd.ckpt_end ? __ldg(p.ckpt_pos + c_next) : -1;
   bool signaled = false;  // the prompt's ready counter has this block's arrival
 
   for (int c = 0; c < nchunks && ok; ++c) {
@@ -667,7 +670,7 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
       }
 
       const int pos = t0 + L;
-      const bool emit = c_next < sd.ckpt_end && p.ckpt_pos[c_next] == pos;
+      const bool emit = ck_pos == pos;
       const bool last = c + 1 == nchunks;
       const float nd = last ? 1.f : sm.next_decay;
       // (only the d x d state is stored: rows and columns past d are zero)
@@ -719,7 +722,10 @@ chunked_prefill_kernel(const __grid_constant__ ChunkedParams P) {
           tmem_st16(t_lane + TM_S32 + 64 * half + c0 + 16, hi);
         }
       }
-      if (emit) ++c_next;
+      if (emit) {
+        ++c_next;
+        ck_pos = c_next < sd.ckpt_end ? __ldg(p.ckpt_pos + c_next) : -1;
+      }
       tmem_st_wait();
       const bool tma_out = L == kC && dh == kD;  // whole d = 128 chunks leave by TMA
       if (tma_out) fence_proxy_async_smem();

@@ -616,6 +616,9 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
     }
     __syncwarp();
     int c_next = sd.ckpt_begin;
+    // the next checkpoint's position (-1: none left), read again only after a checkpoint is
+    // stored, so that no chunk waits on a global load to decide
+    int ck_pos = c_next < sd.ckpt_end ? __ldg(p.ckpt_pos + c_next) : -1;
 
     for (int c = 0; c < nchunks && ok; ++c) {
       const int b = c & 1, t0 = c * kC, L = min(kC, sd.len - t0);
@@ -678,7 +681,7 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
       bool last_ckpt = false;  // this chunk stores the unit's last checkpoint
       {
         const int pos = t0 + L;
-        const bool emit = c_next < sd.ckpt_end && p.ckpt_pos[c_next] == pos;
+        const bool emit = ck_pos == pos;
         const float nd = last ? 1.f : sm.gamma[b ^ 1];
         // (only the d x d state is stored: rows and columns past d are zero)
         const bool store_row = (int)row < dh;
@@ -722,7 +725,10 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
             tmem_st16(t_lane + TM_S32 + 64 * half + c0 + 16, hi);
           }
         }
-        if (emit) ++c_next;
+        if (emit) {
+          ++c_next;
+          ck_pos = c_next < sd.ckpt_end ? __ldg(p.ckpt_pos + c_next) : -1;
+        }
         last_ckpt = emit && c_next == sd.ckpt_end;
         tmem_st_wait();
       }
