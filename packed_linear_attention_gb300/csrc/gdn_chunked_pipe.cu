@@ -186,25 +186,19 @@ __device__ __forceinline__ void commit(Smem& sm, int i) {
 // significand) leaves T within about 1e-6 relative, far below the fp16
 // rounding of the operands built from T. Only the lower triangle and the unit diagonal of
 // T are written; blocks of T above the diagonal are never read.
-// Every block of T is also written, as soon as it is known, into the fp16 operands
-// T1 = T diag(c1) and T2 = T diag(c2) (column factors c1, c2; 128B-swizzled 64 x 64 tiles
-// whose blocks above the diagonal are zero).
+// T is also written into the fp16 operands T1 = T diag(c1) and T2 = T diag(c2) (column
+// factors c1, c2; 128B-swizzled 64 x 64 tiles whose blocks above the diagonal are zero):
+// the two diagonal 32 x 32 blocks by every prep warp once the first level is done, the
+// block below them straight from the last product's accumulator.
 // Step 1: one prep warp inverts diagonal blocks 2 pair and 2 pair + 1 (pair 0 or 1; lanes
 // 0-15 the first block, 16-31 the second) while the other prep warps do independent work.
-__device__ __forceinline__ void invert_diag_blocks(const float* A, float* T, uint8_t* T1,
-                                                   uint8_t* T2, const float* c1,
-                                                   const float* c2, int pair, int lane) {
+__device__ __forceinline__ void invert_diag_blocks(const float* A, float* T, int pair,
+                                                   int lane) {
   const int o = 16 * (2 * pair + (lane >> 4)), j = lane & 15;
   float x[16];
   diag_block_column_rl(A, o, j, x);
-  const float f1 = c1[o + j], f2 = c2[o + j];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    T[(o + i) * kLd + o + j] = x[i];
-    const uint32_t off = sw128_offset(o + i, o + j, 64);
-    *reinterpret_cast<__half*>(T1 + off) = __float2half_rn(x[i] * f1);
-    *reinterpret_cast<__half*>(T2 + off) = __float2half_rn(x[i] * f2);
-  }
+  for (int i = 0; i < 16; ++i) T[(o + i) * kLd + o + j] = x[i];
 }
 
 // Step 2 (all prep warps), after the diagonal blocks are in T. Ends with T1/T2 published
@@ -223,7 +217,6 @@ __device__ void invert_merge(const float* A, float* T, float* X, uint8_t* T1, ui
     float y[4] = {0.f, 0.f, 0.f, 0.f};
     tile_mm(y, T + r0 * kLd + r0, kLd, 0, xs, kLdXs, 0, 0, 16, gid, tig);
     tile_store(T, kLd, r0, n0, y, -1.f, gid, tig);
-    tile_store_t12(T1, T2, r0, n0, y, c1, c2, gid, tig);
   }
   named_sync(kBarPrep, kGroup);
   // 32 -> 64: X = A[32:64, 0:32] T[0:32, 0:32], then T[32:64, 0:32] = -T[32:64, 32:64] X;
@@ -233,6 +226,37 @@ __device__ void invert_merge(const float* A, float* T, float* X, uint8_t* T1, ui
     const int r0 = 16 * mt, n0 = 8 * nt;
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     tile_mm(d, A + 32 * kLd, kLd, r0, T, kLd, n0, nt >= 2 ? 16 : 0, 32, gid, tig);
+    // while the warp MMAs run: the two diagonal 32 x 32 blocks of T1/T2, final after the
+    // first level. A thread takes 8 columns of one row (warps 0-3 the first block, 4-7 the
+    // second); the 8 lanes of each quarter warp take 8 consecutive rows at the same
+    // columns, so that their float4 reads of T fall on distinct banks.
+    {
+      const int bk = warp >> 2, i = 32 * bk + 8 * (warp & 3) + (lane & 7);
+      const int j0 = 32 * bk + 8 * (lane >> 3);
+      float x1[8], x2[8];
+#pragma unroll
+      for (int q4 = 0; q4 < 8; q4 += 4) {
+        const int j = j0 + q4;
+        const float4 tv = *reinterpret_cast<const float4*>(T + i * kLd + j);
+        const float4 gv = *reinterpret_cast<const float4*>(c1 + j);
+        const float4 bv = *reinterpret_cast<const float4*>(c2 + j);
+        const float t4[4] = {tv.x, tv.y, tv.z, tv.w}, g4[4] = {gv.x, gv.y, gv.z, gv.w},
+                    b4[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+        for (int f = 0; f < 4; f += 2) {
+          const float2 tij = make_float2(j + f <= i ? t4[f] : 0.f,  // zero above the diagonal
+                                         j + f + 1 <= i ? t4[f + 1] : 0.f);
+          const float2 y1 = mul2(tij, make_float2(g4[f], g4[f + 1]));
+          const float2 y2 = mul2(tij, make_float2(b4[f], b4[f + 1]));
+          x1[q4 + f] = y1.x;
+          x1[q4 + f + 1] = y1.y;
+          x2[q4 + f] = y2.x;
+          x2[q4 + f + 1] = y2.y;
+        }
+      }
+      st_chunk(T1, i, j0, 64, x1);
+      st_chunk(T2, i, j0, 64, x2);
+    }
     tile_store(X, kLdX, r0, n0, d, 1.f, gid, tig);
   }
   named_sync(kBarPrep, kGroup);
@@ -428,7 +452,7 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
       // columns 32-63, blocks 2 and 3), so they start without waiting for the other warps.
       if (warp == 0 || warp == 5) {
         __syncwarp();
-        invert_diag_blocks(sA, sT, sT1, sT2, f.BG, f.B, warp == 0 ? 0 : 1, lane);
+        invert_diag_blocks(sA, sT, warp == 0 ? 0 : 1, lane);
       } else {  // M1 has consumed Q
         const int rank = warp < 5 ? warp - 1 : warp - 2;  // 0-5 over warps 1-4, 6, 7
         for (int idx = 32 * rank + lane; idx < 1024; idx += kGroup - 64) {
@@ -643,9 +667,12 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
           const float d8[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
           float x[8], y[8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
+          for (int q = 0; q < 8; q += 2) {
             x[q] = __uint_as_float(r[e + q]);
-            y[q] = x[q] * d8[q];
+            x[q + 1] = __uint_as_float(r[e + q + 1]);
+            const float2 t = mul2(make_float2(x[q], x[q + 1]), make_float2(d8[q], d8[q + 1]));
+            y[q] = t.x;
+            y[q + 1] = t.y;
           }
           st_chunk(sD, row, 32 * half + e, 128, x);
           st_chunk(sDp, row, 32 * half + e, 128, y);
@@ -717,9 +744,17 @@ chunked_pipe_kernel(const __grid_constant__ ChunkedParams P) {
           } else {
             uint32_t lo[16], hi[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              lo[e] = __float_as_uint(__uint_as_float(s32[e]) * nd);
-              hi[e] = __float_as_uint(__uint_as_float(s32[16 + e]) * nd);
+            for (int e = 0; e < 16; e += 2) {
+              const float2 a = mul2(
+                  make_float2(__uint_as_float(s32[e]), __uint_as_float(s32[e + 1])),
+                  make_float2(nd, nd));
+              const float2 bq = mul2(
+                  make_float2(__uint_as_float(s32[16 + e]), __uint_as_float(s32[17 + e])),
+                  make_float2(nd, nd));
+              lo[e] = __float_as_uint(a.x);
+              lo[e + 1] = __float_as_uint(a.y);
+              hi[e] = __float_as_uint(bq.x);
+              hi[e + 1] = __float_as_uint(bq.y);
             }
             tmem_st16(t_lane + TM_S32 + 64 * half + c0, lo);
             tmem_st16(t_lane + TM_S32 + 64 * half + c0 + 16, hi);
