@@ -317,6 +317,10 @@ gdn_status gdn_prefill_async_join(gdn_handle* handle, void* stream);
  *     a[b], beta[b] ([batch][H_v] fp32); o[b] ([batch][H_v][d] io_dtype) = scale * S_new q
  *  slot_idx_dev     [batch] int32 device array of distinct slot indices in [0, num_slots).
  * Distinct slots are the caller's duty (two batch rows naming one slot race).
+ * The call checks its arguments on the host and enqueues one kernel on `stream`, with no
+ * copy and no allocation, so a serving loop can capture it in a CUDA graph and replay it
+ * (the graph then keeps the buffer addresses of the capture; a test replays captured
+ * steps and matches direct calls bit for bit).
  * Errors: INVALID_ARGUMENT, UNSUPPORTED, CUDA. */
 gdn_status gdn_decode_step(gdn_handle* handle, const gdn_config* cfg, int32_t batch,
                            const void* q, const void* k, const void* v,

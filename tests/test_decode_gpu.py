@@ -82,3 +82,45 @@ def test_mixed_step_prefill_plus_decode():
     od, pool = _decode_gpu(ms, np.arange(B), ms.dec_states.copy(), torch)
     assert_close(od, ro1[pre.total_tokens:], "bf16", "decode vs oracle")
     assert_close(pool, rf1[pre.num_seqs:], "bf16", "decode states vs oracle")
+
+
+def test_decode_steps_replay_from_a_cuda_graph():
+    """Decode steps captured once in a CUDA graph and replayed: the call does its checks on
+    the host and enqueues one kernel, so the graph holds the whole step. Three replays
+    after the capture give the same o and states, bit for bit, as three direct calls."""
+    torch = torch_cuda()
+    ms = I.mixed_step()
+    cfg = gdn.make_config(16, 32, 128)
+    B = ms.dec_q.shape[0]
+    rng = np.random.default_rng(5)
+    S = B + 3
+    pool0 = np.zeros((S, 32, 128, 128), np.float32)
+    slots = rng.permutation(S)[:B].astype(np.int32)
+    pool0[slots] = ms.dec_states
+    q, k, v = (_bf16_dev(x, torch) for x in (ms.dec_q, ms.dec_k, ms.dec_v))
+    a, b = torch.from_numpy(ms.dec_a).cuda(), torch.from_numpy(ms.dec_beta).cuda()
+    slot_t = torch.from_numpy(slots).cuda()
+
+    def steps(pool, o, n, stream=None):
+        for _ in range(n):
+            gdn.gdn_decode_step(handle(), cfg, B, q, k, v, a, b, pool, S, slot_t, o, stream)
+
+    direct_pool = torch.from_numpy(pool0.copy()).cuda()
+    direct_o = torch.empty((B, 32, 128), dtype=torch.bfloat16, device="cuda")
+    steps(direct_pool, direct_o, 3)
+    torch.cuda.synchronize()
+
+    graph_pool = torch.from_numpy(pool0.copy()).cuda()
+    graph_o = torch.empty((B, 32, 128), dtype=torch.bfloat16, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):  # the capture runs no step; replays do
+        with torch.cuda.graph(g, stream=side):
+            steps(graph_pool, graph_o, 1, side)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(graph_o, direct_o)
+    assert torch.equal(graph_pool, direct_pool)
