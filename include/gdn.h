@@ -175,6 +175,7 @@ gdn_status gdn_prefill_workspace_size(const gdn_config* cfg, int32_t num_seqs,
  *                   is their initial state and they emit no output.
  *  q, k             [T][H_k][d] io_dtype.   v: [T][H_v][d] io_dtype.
  *  a, beta          [T][H_v] fp32: log-decay (g = exp(a), a <= 0) and the write strength.
+ *                   a = -inf (g = 0) is allowed: the state restarts at that token.
  *  initial_state    [N][H_v][d][d] fp32, or NULL for all-zero initial states.
  *  ckpt_cu_host     [N+1] int32 CSR over ckpt_pos_host (ckpt_cu[0] = 0), or NULL when no
  *                   prompt asks for a checkpoint.

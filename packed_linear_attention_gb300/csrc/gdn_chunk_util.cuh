@@ -25,6 +25,8 @@ constexpr int kLdXs = 12;       // row stride of a warp's 16 x 8 merge scratch (
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr int kStatusTimeout = 5;  // GDN_ERR_DEVICE_TIMEOUT
 constexpr float kLog2e = 1.4426950408889634f;
+// Lowest log2-decay of one token in the chunk scan (see gate_scan).
+constexpr float kMinLog2Decay = -200.f;
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -117,8 +119,11 @@ struct Factors {
 // its own (no contraction), so that every caller, in either schedule, gets the same bits.
 __device__ __forceinline__ float gate_scan(const float (&g)[4], int lane, float& a0,
                                            float& a1) {
-  a0 = __fmul_rn(g[0], kLog2e);
-  a1 = __fmul_rn(g[1], kLog2e);
+  // A token's log2-decay is held at -200 or above: a = -inf (g = 0, the state restarts at
+  // that token) then gives factors 2^-200, which are exactly 0 in fp32, and no inf - inf in
+  // the differences of the scan. Decays above -200 (a > -138.6) keep their bits.
+  a0 = fmaxf(__fmul_rn(g[0], kLog2e), kMinLog2Decay);
+  a1 = fmaxf(__fmul_rn(g[1], kLog2e), kMinLog2Decay);
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const float y0 = __shfl_up_sync(0xffffffffu, a0, off);
