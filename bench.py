@@ -69,14 +69,14 @@ MEASURED_TRAFFIC = {
         "packed_linear_attention_gb300/csrc/gdn_chunked.cu":
             "05dc96bf04958dee87460f0491551d5acece8a6a2563109877897692fb3072a8",
         "packed_linear_attention_gb300/csrc/gdn_chunk_util.cuh":
-            "92633a3576a4cac7806eace0e638f52b98ad447f585909d4c542593632791654",
+            "79a2646b770efccd02ab41cc732b8ffe6c5c890479fc9c579353bcf415d15a2f",
         "packed_linear_attention_gb300/csrc/ptx_sm103.cuh":
             "762c9e7ef68fa3e883aaeb592d47ce09eed2b387cc7b6e46fa74fa53d9b1da60",
         "packed_linear_attention_gb300/csrc/gdn_tma.cu":
             "b97a465a15c3850359ec63c6925ea5d4f1962a058db1f247ccd5c0a9055e72f2",
     },
     "read_bytes": 545.9e6,
-    "write_bytes": 356.7e6,
+    "write_bytes": 356.8e6,
 }
 
 
