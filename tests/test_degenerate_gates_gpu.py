@@ -1,8 +1,10 @@
-"""The gates' degenerate cases against the oracle, in every kernel: no decay (a = 0,
+"""Degenerate inputs against the oracle, in every kernel. The gates: no decay (a = 0,
 g = 1) with full writes (beta = 1); pure decay (beta = 0, the state only shrinks); a
 memoryless token (a = -inf, g = 0: the state restarts from that token's write); and decays
 strong enough that exp(a) underflows fp32 (a = -120). Gated Delta Networks (Yang, Kautz &
-Hatamizadeh, 2024) define the update for every g in [0, 1] and beta in [0, 1]."""
+Hatamizadeh, 2024) define the update for every g in [0, 1] and beta in [0, 1]. The keys
+and queries: no in-kernel L2 norm (rows normalised upstream), and all-zero rows (norm 0,
+the epsilon under the root)."""
 from __future__ import annotations
 
 import dataclasses
@@ -48,6 +50,31 @@ def _pack(case: str) -> I.Pack:
 @pytest.mark.parametrize("pref", KERNELS)
 def test_degenerate_gates(case, pref):
     p = _pack(case)
+    got = run(p, pref)
+    assert all(np.isfinite(x).all() for x in got), "non-finite output"
+    compare_units(p, got, list(range(len(LENS))), list(range(CFG["num_v_heads"])))
+
+
+def _qk_pack(case: str) -> I.Pack:
+    p = I.make_pack(LENS, **CFG, io_dtype="bf16", seed=53, init_std=0.02,
+                    ckpt_lists=[[64, 192], [64], [128, 131], [1], [], [256, 257]])
+    if case == "no_l2norm":  # q and k normalised upstream (the generator's own rows)
+        return dataclasses.replace(p, qk_l2norm=False, name=f"{p.name}_{case}")
+    if case == "zero_rows":  # all-zero q and k rows (norm 0: the epsilon under the root)
+        q, k = p.q.copy(), p.k.copy()
+        rng = np.random.default_rng(9)
+        zq = rng.random(q.shape[:2]) < 0.05
+        zk = rng.random(k.shape[:2]) < 0.05
+        q[zq] = 0
+        k[zk] = 0
+        return dataclasses.replace(p, q=q, k=k, name=f"{p.name}_{case}")
+    raise ValueError(case)
+
+
+@pytest.mark.parametrize("case", ["no_l2norm", "zero_rows"])
+@pytest.mark.parametrize("pref", KERNELS)
+def test_qk_without_norm_and_zero_rows(case, pref):
+    p = _qk_pack(case)
     got = run(p, pref)
     assert all(np.isfinite(x).all() for x in got), "non-finite output"
     compare_units(p, got, list(range(len(LENS))), list(range(CFG["num_v_heads"])))
