@@ -4,7 +4,8 @@ memoryless token (a = -inf, g = 0: the state restarts from that token's write); 
 strong enough that exp(a) underflows fp32 (a = -120). Gated Delta Networks (Yang, Kautz &
 Hatamizadeh, 2024) define the update for every g in [0, 1] and beta in [0, 1]. The keys
 and queries: no in-kernel L2 norm (rows normalised upstream), and all-zero rows (norm 0,
-the epsilon under the root)."""
+the epsilon under the root). Sequence splitting over memoryless tokens, and the decode
+step with such inputs."""
 from __future__ import annotations
 
 import dataclasses
@@ -12,10 +13,11 @@ import dataclasses
 import numpy as np
 import pytest
 
+from oracle import ref
 from packed_linear_attention_gb300 import gdn
 from packed_linear_attention_gb300 import inputs as I
 
-from gpu_util import compare_units, run
+from gpu_util import assert_close, compare_units, handle, run, torch_cuda
 
 pytestmark = pytest.mark.gpu
 
@@ -78,3 +80,49 @@ def test_qk_without_norm_and_zero_rows(case, pref):
     got = run(p, pref)
     assert all(np.isfinite(x).all() for x in got), "non-finite output"
     compare_units(p, got, list(range(len(LENS))), list(range(CFG["num_v_heads"])))
+
+
+def test_split_with_memoryless_tokens():
+    """Sequence splitting over memoryless tokens: the segment maps (zero and identity
+    starts) restart at a = -inf inside a segment, and their composition stays exact."""
+    torch = torch_cuda()
+    h = handle()
+    p = _pack("memoryless_tokens")
+    buf = gdn.to_device(p)
+    gdn.prefill_split(h, buf, 64)  # the 257-token prompt in five segments
+    torch.cuda.synchronize()
+    assert gdn.gdn_read_device_status(buf.split_workspace) == 0
+    got = (buf.o.float().cpu().numpy().astype(np.float64),
+           buf.ckpt.cpu().numpy().astype(np.float64),
+           buf.final.cpu().numpy().astype(np.float64))
+    assert all(np.isfinite(x).all() for x in got), "non-finite output"
+    compare_units(p, got, list(range(len(LENS))), list(range(CFG["num_v_heads"])))
+
+
+def test_decode_step_degenerate_inputs():
+    """One decode token with a = -inf (the stored state is dropped), beta = 0 (only the
+    decay applies) and all-zero q or k rows, against the oracle."""
+    torch = torch_cuda()
+    ms = I.mixed_step()
+    B = ms.dec_q.shape[0]
+    q, k, a, b = ms.dec_q.copy(), ms.dec_k.copy(), ms.dec_a.copy(), ms.dec_beta.copy()
+    a[0::4] = -np.inf
+    b[1::4] = 0.0
+    q[2::4, 0] = 0
+    k[3::4, 1] = 0
+    cfg = gdn.make_config(16, 32, 128)
+    slots = np.arange(B, dtype=np.int32)[::-1].copy()
+    pool_np = np.ascontiguousarray(ms.dec_states[::-1])
+    pool = torch.from_numpy(pool_np.copy()).cuda()
+    o = torch.empty((B, 32, 128), dtype=torch.bfloat16, device="cuda")
+    dev = lambda x: torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)  # noqa
+    gdn.gdn_decode_step(handle(), cfg, B, dev(q), dev(k), dev(ms.dec_v), torch.from_numpy(a).cuda(),
+                        torch.from_numpy(b).cuda(), pool, B, torch.from_numpy(slots).cuda(), o)
+    torch.cuda.synchronize()
+    f = I.bf16_bits_to_f32
+    ro, rpool = ref.decode(f(q), f(k), f(ms.dec_v), a, b, pool_np, slots, scale=128 ** -0.5)
+    go = o.float().cpu().numpy().astype(np.float64)
+    gp = pool.cpu().numpy().astype(np.float64)
+    assert np.isfinite(go).all() and np.isfinite(gp).all()
+    assert_close(go, ro, "bf16", "decode o")
+    assert_close(gp, rpool, "bf16", "decode states")
