@@ -83,3 +83,44 @@ def test_snapshot_pool_bounds():
                                          buf.ckpt, buf.final, size - 16, buf.workspace,
                                          buf.workspace_bytes, raise_on_error=False)
     assert st == gdn.GDN_ERR_POOL_EXHAUSTED
+
+
+@pytest.mark.parametrize("pref", [gdn.KERNEL_CHUNKED_PIPELINED, gdn.KERNEL_CHUNKED_THROUGHPUT])
+def test_snapshot_copies_finish_after_a_device_timeout(pref):
+    """With the test hook, every unit's first copy wait runs out. Each block still counts
+    its prompt's arrival, so the side stream's waits end and the copies finish (polled
+    here with a deadline, never waited on without one); the status word reports the
+    timeout, and the next snapshot call on the same context is right."""
+    import time
+    torch = torch_cuda()
+    h = handle()
+    p = I.make_pack([200, 64, 5, 0], num_k_heads=2, num_v_heads=4, head_dim=128,
+                    io_dtype="bf16", seed=43, init_std=0.02,
+                    ckpt_lists=[[64, 200], [64], [5], []])
+    buf = gdn.to_device(p)
+    gdn.gdn_set_kernel_preference(h, pref)
+    gdn.gdn_set_test_hook(h, 1)
+    try:
+        gdn.prefill_snapshot(h, buf, 0)
+        deadline = time.monotonic() + 60.0
+        while not gdn.gdn_checkpoint_copy_query(h):
+            assert time.monotonic() < deadline, "the checkpoint copies never finished"
+            time.sleep(0.01)
+        status = gdn.gdn_read_device_status(buf.workspace)
+    finally:
+        gdn.gdn_set_test_hook(h, 0)
+        gdn.gdn_set_kernel_preference(h, gdn.KERNEL_AUTO)
+    assert status == gdn.GDN_ERR_DEVICE_TIMEOUT
+    want = run(p, pref)
+    nbytes = buf.ckpt.numel() * 4
+    pool = _pool_view(torch, h, nbytes, 0)
+    gdn.gdn_set_kernel_preference(h, pref)
+    try:
+        gdn.prefill_snapshot(h, buf, 0)
+        gdn.gdn_checkpoint_copy_wait(h)
+        torch.cuda.synchronize()
+    finally:
+        gdn.gdn_set_kernel_preference(h, gdn.KERNEL_AUTO)
+    assert gdn.gdn_read_device_status(buf.workspace) == 0
+    np.testing.assert_array_equal(buf.ckpt.cpu().numpy().astype(np.float64), want[1])
+    np.testing.assert_array_equal(pool.view(np.float32).reshape(buf.ckpt.shape), want[1])
